@@ -1,0 +1,555 @@
+#!/usr/bin/env python
+"""Benchmark of one Windowed-MTP speculative-decoding attention step on GB300.
+
+A step is the whole hot path over one batch: d draft steps (ring append +
+sink/window draft attention, each with its split merge) and the verification
+attention of T = d + 1 positions over the full bf16 KV cache (+ merge), then a
+rollback of the d speculative ring entries so every timed step sees the same
+state.  It runs as one CUDA graph; the L2 is flushed between timed steps.
+
+Default workload: 1M-token context, full-attention layer of a hybrid target
+(GQA 8, head_dim 256, S=4, W=4096), draft depth 3.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from speculative_decoding_attention_gb300 import inputs as wm_inputs  # noqa: E402
+from speculative_decoding_attention_gb300 import workloads  # noqa: E402
+
+METRIC = "decode-attn µs/step & HBM GB/s (% roofline): windowed draft vs full verify, 1M"
+UNIT = "us/step"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
+KERNEL_SOURCES = ("attn_kernel.cuh", "ptx.cuh", "wm_internal.h")
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default=workloads.BENCH_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--depth", type=int, default=None, help="draft depth d (verify T = d + 1)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p))
+        except ValueError:
+            pass
+    return {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        path = os.path.join(ROOT, "speculative_decoding_attention_gb300", "csrc", name)
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, depth: int):
+    """DRAM bytes per verify launch from the committed ncu summary, if it was
+    taken on the current kernel source for this workload; else None."""
+    try:
+        rec = json.load(open(PROFILE_TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_hash") != kernel_source_hash():
+        return None
+    entry = rec.get("workloads", {}).get(f"{workload}/d{depth}")
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        try:
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:  # older torch: fall back to the ordinal
+            self.gpu = str(device.index or 0)
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i - 5] for r in rows for i in range(5, 9) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device state of one workload and its captured step."""
+
+    def __init__(self, w: workloads.Workload, depth: int, device):
+        from speculative_decoding_attention_gb300 import wm
+
+        self.wm, self.w, self.d, self.T, self.dev = wm, w, depth, depth + 1, device
+        self.inp = wm_inputs.make_inputs(w, depth=depth, device=device)
+        inp = self.inp
+        self.kv = wm.KVCache(inp.k, inp.v, inp.seq_lens, inp.block_table)
+        self.ring = wm.Ring.create(w.batch, w.n_kv_heads, w.head_dim, w.sink, w.window, device)
+        self._build_ring()
+        B, Hq, D = w.batch, w.n_q_heads, w.head_dim
+        self.base_len = inp.seq_lens.clone()
+        self.d_out = torch.empty((depth, B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.d_lse = torch.empty((depth, B, Hq), dtype=torch.float32, device=device)
+        self.v_out = torch.empty_like(inp.q_verify)
+        self.v_lse = torch.empty(inp.q_verify.shape[:3], dtype=torch.float32, device=device)
+        self.d_splits = wm.plan_splits(wm.WM_OP_DRAFT, B, w.n_kv_heads, Hq, 1, D, w.slots)
+        self.v_splits = wm.plan_splits(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
+        dws = wm.workspace_size(wm.WM_OP_DRAFT, B, w.n_kv_heads, Hq, 1, D, w.slots)
+        vws = wm.workspace_size(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
+        self.d_ws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
+        self.v_ws = torch.empty(max(vws, 256), dtype=torch.uint8, device=device)
+        self.graph = None
+        self.ev = None
+
+    def _build_ring(self):
+        wm, w, inp = self.wm, self.w, self.inp
+        tail = w.ring_appends
+        if tail:
+            lens = inp.seq_lens - tail
+            wm.ring_fill(self.ring, wm.KVCache(inp.k, inp.v, lens, inp.block_table))
+            for t in range(tail):
+                kj, vj = inp.position_rows([n - tail + t for n in inp.seq_lens_host])
+                wm.ring_append(self.ring, kj.contiguous(), vj.contiguous())
+        else:
+            wm.ring_fill(self.ring, self.kv)
+
+    def launches_per_step(self) -> int:
+        per_draft = 2 + (1 if self.d_splits > 1 else 0)
+        return self.d * per_draft + 1 + (1 if self.v_splits > 1 else 0) + 1
+
+    def run(self, ev=None):
+        wm, w, inp = self.wm, self.w, self.inp
+        if ev:
+            ev[0].record()
+        for j in range(self.d):
+            wm.ring_append(self.ring, inp.k_new[j], inp.v_new[j])
+            wm.draft_attn(self.ring, inp.q_draft[j], w.scale, out=self.d_out[j], lse=self.d_lse[j],
+                          workspace=self.d_ws)
+        if ev:
+            ev[1].record()
+        wm.verify_attn(self.kv, inp.q_verify, w.scale, out=self.v_out, lse=self.v_lse, workspace=self.v_ws)
+        if ev:
+            ev[2].record()
+        wm.ring_rollback(self.ring, self.base_len)
+
+    def capture(self):
+        self.run()  # eager once: kernel attributes, descriptors, first-touch
+        torch.cuda.synchronize()
+        try:
+            self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        except TypeError:
+            self.ev = None
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            self.run(self.ev)
+        torch.cuda.synchronize()
+
+
+def gpu_arm(args, rank, world, local):
+    from speculative_decoding_attention_gb300 import build as wm_build
+    from speculative_decoding_attention_gb300 import wm
+
+    if not os.path.exists(wm_build.LIB) or not wm_build.up_to_date():
+        wm_build.build()
+    wm.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    w = workloads.get(args.workload)
+    depth = args.depth if args.depth is not None else (
+        workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)
+
+    st = Step(w, depth, device)
+    st.capture()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        st.graph.replay()
+    torch.cuda.synchronize()
+    if wm.get_device_error():
+        raise RuntimeError("device error during warm-up")
+
+    step_ms, draft_ms, verify_ms = [], [], []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record()
+            st.graph.replay()
+            e1.record()
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            if st.ev:
+                draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
+                verify_ms.append(st.ev[1].elapsed_time(st.ev[2]))
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = clk.summary()
+    if not st.ev:  # no in-graph events: time the verify alone, same way
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record()
+            wm.verify_attn(st.kv, st.inp.q_verify, w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
+            e1.record()
+            e1.synchronize()
+            verify_ms.append(e0.elapsed_time(e1))
+    if wm.get_device_error():
+        raise RuntimeError("device error during the timed steps")
+    out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
+
+    us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
+    us_verify = 1e3 * sum(verify_ms) / len(verify_ms)
+    us_draft = 1e3 * sum(draft_ms) / len(draft_ms) if draft_ms else None
+
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    sum_n = sum(st.inp.seq_lens_host)
+    verify_bytes = 2 * Hkv * D * 2 * sum_n + 2 * (B * st.T * Hq * D * 2) + B * st.T * Hq * 4
+    draft_bytes = 2 * B * Hkv * w.slots * D * 2 + 2 * (B * Hq * D * 2) + B * Hq * 4
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+    achieved = verify_bytes / (us_verify * 1e-6) / 1e9
+    draft_gbs = draft_bytes * depth / (us_draft * 1e-6) / 1e9 if us_draft else None
+
+    e2e = None if args.no_e2e else e2e_leg(st, args, world, device)
+    cpu = None
+    if not args.no_cpu and rank == 0:
+        cpu = cpu_baseline(st, args)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(us_step, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_step / 1e3, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
+        "config": {
+            "workload": w.name,
+            "batch": B, "context": w.context if not w.ragged else list(w.ragged),
+            "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D, "sink": w.sink, "window": w.window,
+            "draft_depth": depth, "verify_positions": st.T, "kv_layout": "paged" if w.page_size else "contiguous",
+            "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+            "l2": "flushed between timed steps (write of 2x L2); each step also reads the full KV cache (> L2)",
+            "execution": "one CUDA graph per step", "parallelism": f"replicas x{world}",
+        },
+        "detail": {
+            "verify_us": round(us_verify, 2),
+            "verify_gbs": round(achieved, 1),
+            "draft_chain_us": None if us_draft is None else round(us_draft, 2),
+            "draft_us_per_step": None if us_draft is None else round(us_draft / depth, 2),
+            "draft_gbs": None if draft_gbs is None else round(draft_gbs, 1),
+            "draft_kv_bytes_per_step": 2 * B * Hkv * w.slots * D * 2,
+            "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
+            "outputs_finite": out_ok,
+            "steps_per_s_all_ranks": round(world * 1e6 / us_step, 1),
+        },
+        "roofline": {
+            "kernel": "attn_kernel (verify, split-KV) + lse_merge",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} hbm_gbs",
+            "traffic": profiled_traffic(w.name, depth),
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def e2e_leg(st: Step, args, world, device) -> dict:
+    """The same step through the public API with host buffers: every step copies
+    its inputs from pinned host memory (draft queries, the appended draft K/V,
+    verify queries, the verify tokens' own K/V into the cache) and reads every
+    output back; eager calls, no graph."""
+    wm, w, inp = st.wm, st.w, st.inp
+    T = st.T
+    host_in = {
+        "q_draft": inp.q_draft.cpu().pin_memory(), "k_new": inp.k_new.cpu().pin_memory(),
+        "v_new": inp.v_new.cpu().pin_memory(), "q_verify": inp.q_verify.cpu().pin_memory(),
+    }
+    contiguous = inp.block_table is None
+    if contiguous:
+        tail = [slice(n - T, n) for n in inp.seq_lens_host]
+        host_in["k_tail"] = torch.stack([inp.k[b, :, tail[b]] for b in range(w.batch)]).cpu().pin_memory()
+        host_in["v_tail"] = torch.stack([inp.v[b, :, tail[b]] for b in range(w.batch)]).cpu().pin_memory()
+    dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in host_in.items()}
+    host_out = {"d_out": torch.empty(st.d_out.shape, dtype=st.d_out.dtype).pin_memory(),
+                "d_lse": torch.empty(st.d_lse.shape, dtype=st.d_lse.dtype).pin_memory(),
+                "v_out": torch.empty(st.v_out.shape, dtype=st.v_out.dtype).pin_memory(),
+                "v_lse": torch.empty(st.v_lse.shape, dtype=st.v_lse.dtype).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        if contiguous:
+            for b, n in enumerate(inp.seq_lens_host):
+                inp.k[b, :, n - T:n].copy_(dev_in["k_tail"][b])
+                inp.v[b, :, n - T:n].copy_(dev_in["v_tail"][b])
+        for j in range(st.d):
+            wm.ring_append(st.ring, dev_in["k_new"][j], dev_in["v_new"][j])
+            wm.draft_attn(st.ring, dev_in["q_draft"][j], w.scale, out=st.d_out[j], lse=st.d_lse[j],
+                          workspace=st.d_ws)
+        wm.verify_attn(st.kv, dev_in["q_verify"], w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
+        wm.ring_rollback(st.ring, st.base_len)
+        host_out["d_out"].copy_(st.d_out, non_blocking=True)
+        host_out["d_lse"].copy_(st.d_lse, non_blocking=True)
+        host_out["v_out"].copy_(st.v_out, non_blocking=True)
+        host_out["v_lse"].copy_(st.v_lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        one()
+    e1.record()
+    e1.synchronize()
+    barrier(world)
+    us = max_over_ranks(1e3 * e0.elapsed_time(e1) / args.steps, world, device)
+    return {"value": round(us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "eager C-ABI calls; KV cache resident, per-step inputs and outputs cross PCIe/C2C"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, depth, inp_host, rows_fraction):
+    """One bounded sample of the step on the host: every draft row of the d
+    draft steps, and an evenly spaced fraction of the verify rows.  Returns
+    (seconds, scale factor to a whole step, description)."""
+    import oracle
+
+    B, Hq, T = w.batch, w.n_q_heads, depth + 1
+    hist = oracle.KV(inp_host["k"], inp_host["v"], inp_host["block_table"])
+    t0 = time.perf_counter()
+    for j in range(depth):
+        pos = [n + j for n in inp_host["lens"]]
+        oracle.draft(hist, inp_host["q_draft"][j], pos, w.sink, w.window, w.scale)
+    t_draft = time.perf_counter() - t0
+    total_rows = B * T * Hq
+    n_rows = max(1, int(round(total_rows * rows_fraction)))
+    rows = [int(round(i * total_rows / n_rows)) for i in range(n_rows)]
+    t1 = time.perf_counter()
+    oracle.verify(hist, inp_host["q_verify"], inp_host["lens"], w.scale, rows=rows)
+    t_verify = time.perf_counter() - t1
+    per_step = t_draft + t_verify * total_rows / n_rows
+    desc = (f"all {B * Hq} draft rows x {depth} draft steps + {n_rows}/{total_rows} verify rows "
+            f"(scaled x{total_rows / n_rows:.2f}) of {w.name}")
+    return t_draft + t_verify, per_step, desc
+
+
+def host_inputs(inp):
+    return {"k": inp.k.cpu(), "v": inp.v.cpu(),
+            "block_table": None if inp.block_table is None else inp.block_table.cpu(),
+            "lens": list(inp.seq_lens_host), "q_draft": inp.q_draft.cpu(), "q_verify": inp.q_verify.cpu()}
+
+
+def pick_fraction(w, depth, inp_host, budget_s):
+    """Verify-row fraction whose oracle time is about ``budget_s`` seconds."""
+    probe = 1.0 / (w.batch * (depth + 1) * w.n_q_heads)
+    secs, _, _ = oracle_sample(w, depth, inp_host, probe)
+    rows_per_s = 1.0 / max(secs, 1e-6)
+    frac = min(1.0, budget_s * rows_per_s / (w.batch * (depth + 1) * w.n_q_heads))
+    return max(probe, frac)
+
+
+def cpu_baseline(st: Step, args) -> dict:
+    import oracle
+
+    inp_host = host_inputs(st.inp)
+    frac = pick_fraction(st.w, st.d, inp_host, budget_s=8.0)
+    secs, per_step, desc = oracle_sample(st.w, st.d, inp_host, frac)
+    return {"value": round(per_step * 1e6, 1), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": desc, "sample_seconds": round(secs, 2)}
+
+
+def reference_arm(args, rank, world, local):
+    """The fp64 CPU oracle on the host cores, on the GPU arm's workload."""
+    import oracle
+
+    if world > 1:
+        init_dist(world, "gloo")
+        if rank != 0:
+            barrier(world)
+            return
+    oracle.build()
+    w = workloads.get(args.workload)
+    depth = args.depth if args.depth is not None else (
+        workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wm_inputs.make_inputs(w, depth=depth, device=gen_dev)
+    inp_host = host_inputs(inp)
+    del inp
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    frac = pick_fraction(w, depth, inp_host, budget_s=budget)
+    for _ in range(args.warmup):
+        oracle_sample(w, depth, inp_host, frac)
+    per_steps, secs_total, desc = [], 0.0, ""
+    for _ in range(args.steps):
+        secs, per_step, desc = oracle_sample(w, depth, inp_host, frac)
+        per_steps.append(per_step)
+        secs_total += secs
+    us = 1e6 * sum(per_steps) / len(per_steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
+        "config": {"workload": w.name, "draft_depth": depth, "verify_positions": depth + 1,
+                   "parallelism": "host cores (OpenMP over rows)"},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        barrier(world)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        reference_arm(args, rank, world, local)
+    else:
+        gpu_arm(args, rank, world, local)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * wm_api.h -- C ABI of the Windowed-MTP decode-attention library (libwm.so).
+ *
+ * The operations are the decode-time attention of one speculative-decoding
+ * step as described in "Windowed-MTP: Removing the Full-Context Draft-KV Tax
+ * at Million-Token Context" (Abstract):
+ *
+ *   - the MTP draft head attends only to a StreamingLLM-style key set, the
+ *     first S positions (attention sinks) plus the W most recent positions,
+ *     held in a compact ring buffer of S + W slots   -> wm_ring_append,
+ *     wm_ring_fill, wm_draft_attn;
+ *   - the target's full-attention verification of the k+1 proposed positions
+ *     over the entire bf16 KV cache stays intact      -> wm_verify_attn;
+ *   - the split-KV partial results of either are combined by a log-sum-exp
+ *     merge                                            -> wm_lse_merge.
+ *
+ * Conventions shared by every entry point
+ *   - Element types: K, V, q and out are bf16 (IEEE binary16-brain, 2 bytes);
+ *     lse and split partials are fp32; positions/lengths int64; tags and page
+ *     indices int32.  Every tensor is dense row-major in the documented shape.
+ *   - Ownership: every pointer is caller-owned DEVICE memory unless stated;
+ *     the library allocates nothing and keeps no per-call state.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream).  Every call only enqueues work on that stream and
+ *     returns without synchronising; positions and lengths are read on the
+ *     device, so sequences of calls can be captured in a CUDA graph.
+ *   - Validation: arguments are checked on the host before anything is
+ *     enqueued; a failing check returns WM_ERR_INVALID_ARG / WM_ERR_UNSUPPORTED
+ *     / WM_ERR_WORKSPACE and enqueues nothing.  A failed launch returns
+ *     WM_ERR_CUDA.
+ *   - Device-side data errors (a negative length, a length beyond the
+ *     capacity, a block-table entry outside the page pool) cannot be seen on
+ *     the host without a synchronisation.  The kernels clamp or skip the bad
+ *     access, record the first such error in a device word and never trap;
+ *     wm_get_device_error() reads and clears that word.
+ *   - GQA: query head h reads KV head floor(h / G), G = n_q_heads / n_kv_heads.
+ *   - Outputs: out is bf16 rounded to nearest-even once; lse is the natural
+ *     log-sum-exp of the scaled logits in fp32.  A row with no key to attend
+ *     to gets out = 0 and lse = -inf.
+ *   - head_dim must be 64, 128 or 256; n_q_heads a multiple of n_kv_heads;
+ *     G * (query positions) at most 64 rows per KV head.
+ */
+#ifndef WM_API_H
+#define WM_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum wm_status {
+    WM_OK = 0,
+    WM_ERR_INVALID_ARG = 1, /* null pointer, bad size or misaligned pointer */
+    WM_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement */
+    WM_ERR_WORKSPACE = 3,   /* workspace missing or smaller than wm_workspace_size() */
+    WM_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+    WM_ERR_DEVICE_DATA = 5  /* reported by wm_get_device_error(): bad device-side data */
+} wm_status;
+
+/* Device error codes recorded by the kernels (read with wm_get_device_error). */
+#define WM_DEVERR_NONE 0
+#define WM_DEVERR_BAD_LENGTH 1   /* negative length/position or one beyond capacity */
+#define WM_DEVERR_BAD_PAGE 2     /* block-table entry outside [0, n_pages) */
+#define WM_DEVERR_TIMEOUT 3      /* a pipeline wait exceeded its iteration limit */
+
+/*
+ * The draft's compact ring buffer (one per draft attention layer).
+ *   k, v     [batch][n_kv_heads][sink + window][head_dim] bf16
+ *   pos_tag  [batch][sink + window] int32: absolute position held by the
+ *            slot, -1 = empty.  Initialise to -1 (all bytes 0xFF).
+ *   n_seen   [batch] int64: number of positions appended so far.
+ *            Initialise to 0.
+ * Slot of position p:  p                      if p < sink,
+ *                      sink + (p - sink) % window   otherwise.
+ * So the ring holds the sinks 0..S-1 and the W most recent positions; every
+ * older non-sink position has been overwritten ("reclaimed").
+ */
+typedef struct wm_ring {
+    void *k;
+    void *v;
+    int32_t *pos_tag;
+    int64_t *n_seen;
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t sink;   /* S >= 0 */
+    int32_t window; /* W >= 1 */
+} wm_ring;
+
+/*
+ * A full-context KV cache (the target's), contiguous or paged.
+ *   contiguous (block_table == NULL):
+ *       k, v  [batch][n_kv_heads][n_cap][head_dim] bf16
+ *   paged (block_table != NULL):
+ *       k, v  [n_pages][n_kv_heads][page_size][head_dim] bf16
+ *       block_table [batch][max_pages] int32: position j of sequence b lives
+ *       in page block_table[b][j / page_size], row j % page_size.
+ *       page_size must be a multiple of the key tile (64 keys for head_dim
+ *       <= 128, 32 for head_dim 256).
+ *   seq_lens [batch] int64: number of valid positions of each sequence.
+ * k and v must be 16-byte aligned.
+ */
+typedef struct wm_kv {
+    const void *k;
+    const void *v;
+    const int64_t *seq_lens;
+    const int32_t *block_table;
+    int64_t n_cap;   /* contiguous: positions per (sequence, head) row */
+    int64_t n_pages; /* paged: pages in the pool */
+    int32_t page_size;
+    int32_t max_pages;
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+} wm_kv;
+
+/*
+ * Append one draft KV entry per sequence (Abstract: the draft's KV is kept in
+ * a compact ring buffer).  For each sequence b, with p = n_seen[b]:
+ * writes k_new[b], v_new[b] into slot(p), sets pos_tag[b][slot(p)] = p and
+ * n_seen[b] = p + 1.
+ *   k_new, v_new  [batch][n_kv_heads][head_dim] bf16.
+ */
+wm_status wm_ring_append(const wm_ring *ring, const void *k_new, const void *v_new, void *stream);
+
+/*
+ * Bulk-initialise the ring from a history store: the result is bit-identical
+ * to appending positions 0 .. hist->seq_lens[b]-1 one at a time to a ring in
+ * its current state whose n_seen is 0.  Slots that would stay unwritten keep
+ * their K/V bytes and get pos_tag = -1.  hist describes the draft's KV by
+ * absolute position (contiguous or paged, same shape rules as wm_kv; its
+ * n_kv_heads and head_dim must equal the ring's).
+ */
+wm_status wm_ring_fill(const wm_ring *ring, const wm_kv *hist, void *stream);
+
+/*
+ * Speculative rollback: forget draft entries at positions >= new_len[b]
+ * (device int64 [batch]).  Sets n_seen[b] = min(n_seen[b], new_len[b]) and
+ * pos_tag = -1 for every slot holding a position >= the new length.  Window
+ * entries that the rejected positions overwrote are not restored; the window
+ * is short until new appends refill it.
+ */
+wm_status wm_ring_rollback(const wm_ring *ring, const int64_t *new_len, void *stream);
+
+/*
+ * Windowed draft attention (Abstract: the draft attends to a sliding window
+ * plus attention sinks only).  For sequence b the query sits at position
+ * p = n_seen[b] - 1 (the entry appended last) and attends to every ring slot
+ * whose tag t satisfies  0 <= t <= p  and  (t < sink  or  t > p - window).
+ *   q    [batch][n_q_heads][head_dim] bf16
+ *   out  [batch][n_q_heads][head_dim] bf16
+ *   lse  [batch][n_q_heads] fp32, may be NULL
+ *   scale  multiplies q.k before the softmax.
+ *   n_split  0 = chosen by the library; else the number of key splits.
+ *   workspace  device scratch of at least wm_workspace_size(WM_OP_DRAFT, ...)
+ *              bytes (may be NULL when that size is 0); 256-byte aligned.
+ */
+wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale,
+                        int32_t n_split, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
+ * Full-context verification attention (Abstract: full-attention verification
+ * left intact).  Query i (0 <= i < n_q) of sequence b sits at position
+ * seq_lens[b] - n_q + i -- the n_q proposed tokens' own K/V are the last n_q
+ * cache entries -- and attends causally to keys 0 .. seq_lens[b] - n_q + i.
+ *   q    [batch][n_q][n_q_heads][head_dim] bf16
+ *   out  [batch][n_q][n_q_heads][head_dim] bf16
+ *   lse  [batch][n_q][n_q_heads] fp32, may be NULL
+ *   n_split, workspace: as for wm_draft_attn with WM_OP_VERIFY.
+ * With n_q = 1 this is the native full-context decode attention.
+ */
+wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_q_heads,
+                         float scale, int32_t n_split, void *out, float *lse, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * Log-sum-exp merge of split partials, per row r:
+ *   M = max_s lse_s,  lse = M + ln sum_s exp(lse_s - M),
+ *   out = sum_s exp(lse_s - lse) * o_s.
+ *   o_parts   [rows][n_parts][head_dim] fp32, each part normalised by its own sum
+ *   lse_parts [rows][n_parts] fp32 natural log; -inf marks an empty part
+ *   out       [rows][head_dim] bf16;  lse_out [rows] fp32, may be NULL.
+ * A row whose parts are all empty gets out = 0, lse = -inf.
+ */
+wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
+                       int32_t head_dim, void *out, float *lse_out, void *stream);
+
+/* Operations for wm_workspace_size / wm_plan_splits. */
+#define WM_OP_DRAFT 0
+#define WM_OP_VERIFY 1
+
+/*
+ * Number of key splits an attention call will use, for a cache holding up to
+ * max_keys positions per sequence (draft: sink + window).  Depends on the
+ * current device's SM count.  Returns 0 on invalid arguments.
+ */
+int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads,
+                       int32_t n_q, int32_t head_dim, int64_t max_keys, int32_t n_split);
+
+/*
+ * Workspace bytes an attention call needs for the same arguments (0 when it
+ * runs unsplit).  For WM_OP_DRAFT pass n_q = 1 and max_keys = sink + window;
+ * for WM_OP_VERIFY, max_keys = n_cap (contiguous) or max_pages * page_size.
+ * Returns (size_t)-1 on invalid arguments.
+ */
+size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads,
+                         int32_t n_q, int32_t head_dim, int64_t max_keys, int32_t n_split);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device.  *code receives a WM_DEVERR_* value; returns WM_OK if it is
+ * WM_DEVERR_NONE, WM_ERR_DEVICE_DATA otherwise, WM_ERR_CUDA if the read failed.
+ */
+wm_status wm_get_device_error(int32_t *code, void *stream);
+
+/* Static description of a status code. */
+const char *wm_status_string(wm_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t wm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WM_API_H */

@@ -1,0 +1,362 @@
+// wm_api.cu -- the C ABI: argument validation, split planning, TMA descriptor
+// encoding and kernel launches.  Declarations and contracts: include/wm_api.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "wm_internal.h"
+#include "../../include/wm_api.h"
+
+namespace wm {
+namespace {
+
+__device__ int32_t g_device_error;  // first device-side data error (WM_DEVERR_*)
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxRows = 64;  // query rows per KV head (4 m-tiles of 16)
+
+int32_t *device_error_ptr() {
+    static int32_t *ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int32_t *>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count() {
+    static int counts[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// A 4-d view [outer][heads][inner][D] of bf16 rows, read in boxes of
+// 64 columns x kKeyTile rows with the 128-byte swizzle.
+bool encode_kv_map(CUtensorMap *map, const void *base, int head_dim, int64_t inner, int heads,
+                   int64_t outer) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t row = (cuuint64_t)head_dim * 2;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)inner, (cuuint64_t)heads, (cuuint64_t)outer};
+    cuuint64_t strides[3] = {row, row * (cuuint64_t)inner, row * (cuuint64_t)inner * (cuuint64_t)heads};
+    cuuint32_t box[4] = {64, (cuuint32_t)kKeyTile, 1, 1};
+    cuuint32_t elem[4] = {1, 1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                              strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+struct SplitPlan {
+    int n_split = 0;
+    int keys_per_split = 0;
+};
+
+// Key splits for `units` (sequence, KV head) pairs over up to max_keys keys:
+// by default one wave of one CTA per SM, never a split smaller than a tile.
+SplitPlan plan_splits(int units, int64_t max_keys, int requested) {
+    SplitPlan pl;
+    const int64_t tiles = std::max<int64_t>(1, (max_keys + kKeyTile - 1) / kKeyTile);
+    int64_t ns = requested;
+    if (ns <= 0) {
+        const int sms = sm_count();
+        ns = std::max<int64_t>(1, (sms > 0 ? sms : 1) / std::max(1, units));
+    }
+    ns = std::min<int64_t>(ns, tiles);
+    const int64_t tps = (tiles + ns - 1) / ns;
+    pl.n_split = (int)((tiles + tps - 1) / tps);
+    pl.keys_per_split = (int)(tps * kKeyTile);
+    return pl;
+}
+
+size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
+    const size_t o = (size_t)rows_total * n_split * head_dim * sizeof(float);
+    const size_t o_aligned = (o + 255) & ~(size_t)255;
+    return o_aligned + (size_t)rows_total * n_split * sizeof(float);
+}
+
+cudaError_t launch_attn_any(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
+                            cudaStream_t st) {
+    switch (p.head_dim) {
+        case 64: return launch_attn_d64(k, v, p, m_tiles, st);
+        case 128: return launch_attn_d128(k, v, p, m_tiles, st);
+        case 256: return launch_attn_d256(k, v, p, m_tiles, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+bool ring_ok(const wm_ring *r) {
+    return r && r->k && r->v && r->pos_tag && r->n_seen && r->batch > 0 && r->n_kv_heads > 0 &&
+           head_dim_ok(r->head_dim) && r->sink >= 0 && r->window >= 1 &&
+           (int64_t)r->sink + r->window <= INT32_MAX / 2 && aligned(r->k, 16) && aligned(r->v, 16) &&
+           aligned(r->pos_tag, 4) && aligned(r->n_seen, 8);
+}
+
+// Shape checks of a contiguous or paged store; `need_tile_pages` enforces the
+// attention kernel's page rule (whole key tiles per page).
+wm_status kv_check(const wm_kv *kv, bool need_tile_pages) {
+    if (!kv || !kv->k || !kv->v || !kv->seq_lens || kv->batch <= 0 || kv->n_kv_heads <= 0)
+        return WM_ERR_INVALID_ARG;
+    if (!head_dim_ok(kv->head_dim)) return WM_ERR_UNSUPPORTED;
+    if (!aligned(kv->k, 16) || !aligned(kv->v, 16) || !aligned(kv->seq_lens, 8)) return WM_ERR_INVALID_ARG;
+    if (kv->block_table) {
+        if (kv->page_size <= 0 || kv->max_pages <= 0 || kv->n_pages <= 0 || !aligned(kv->block_table, 4))
+            return WM_ERR_INVALID_ARG;
+        if (need_tile_pages && kv->page_size % kKeyTile) return WM_ERR_UNSUPPORTED;
+        if (kv->n_pages > INT32_MAX) return WM_ERR_UNSUPPORTED;
+    } else if (kv->n_cap <= 0 || kv->n_cap > INT32_MAX) {
+        return kv->n_cap <= 0 ? WM_ERR_INVALID_ARG : WM_ERR_UNSUPPORTED;
+    }
+    return WM_OK;
+}
+
+wm_status launch_status(cudaError_t e) { return e == cudaSuccess ? WM_OK : WM_ERR_CUDA; }
+
+}  // namespace
+}  // namespace wm
+
+using namespace wm;
+
+extern "C" {
+
+const char *wm_status_string(wm_status s) {
+    switch (s) {
+        case WM_OK: return "ok";
+        case WM_ERR_INVALID_ARG: return "invalid argument";
+        case WM_ERR_UNSUPPORTED: return "unsupported shape or layout";
+        case WM_ERR_WORKSPACE: return "workspace missing or too small";
+        case WM_ERR_CUDA: return "CUDA error";
+        case WM_ERR_DEVICE_DATA: return "bad device-side data";
+    }
+    return "unknown status";
+}
+
+int32_t wm_version(void) { return 100; }
+
+int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
+                       int32_t head_dim, int64_t max_keys, int32_t n_split) {
+    if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY) || batch <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 ||
+        n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
+        return 0;
+    return plan_splits(batch * n_kv_heads, max_keys, n_split).n_split;
+}
+
+size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
+                         int32_t head_dim, int64_t max_keys, int32_t n_split) {
+    const int32_t ns = wm_plan_splits(op, batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split);
+    if (ns <= 0) return (size_t)-1;
+    if (ns == 1) return 0;
+    return partial_bytes((int64_t)batch * n_q * n_q_heads, ns, head_dim);
+}
+
+wm_status wm_get_device_error(int32_t *code, void *stream) {
+    if (!code) return WM_ERR_INVALID_ARG;
+    int32_t *p = device_error_ptr();
+    if (!p) return WM_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return WM_ERR_CUDA;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return WM_ERR_CUDA;
+    const int32_t zero = 0;
+    if (v != 0 && cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return WM_ERR_CUDA;
+    *code = v;
+    return v == WM_DEVERR_NONE ? WM_OK : WM_ERR_DEVICE_DATA;
+}
+
+wm_status wm_ring_append(const wm_ring *ring, const void *k_new, const void *v_new, void *stream) {
+    if (!ring_ok(ring) || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))
+        return WM_ERR_INVALID_ARG;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    return launch_status(launch_ring_append(ring->k, ring->v, ring->pos_tag, ring->n_seen, ring->batch,
+                                            ring->n_kv_heads, ring->head_dim, ring->sink, ring->window,
+                                            k_new, v_new, err, static_cast<cudaStream_t>(stream)));
+}
+
+wm_status wm_ring_fill(const wm_ring *ring, const wm_kv *hist, void *stream) {
+    if (!ring_ok(ring)) return WM_ERR_INVALID_ARG;
+    const wm_status ks = kv_check(hist, false);
+    if (ks != WM_OK) return ks;
+    if (hist->batch != ring->batch || hist->n_kv_heads != ring->n_kv_heads || hist->head_dim != ring->head_dim)
+        return WM_ERR_INVALID_ARG;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    HistSource h;
+    h.k = hist->k;
+    h.v = hist->v;
+    h.lens = hist->seq_lens;
+    h.block_table = hist->block_table;
+    h.n_cap = hist->n_cap;
+    h.n_pages = hist->n_pages;
+    h.page_size = hist->page_size;
+    h.max_pages = hist->max_pages;
+    return launch_status(launch_ring_fill(ring->k, ring->v, ring->pos_tag, ring->n_seen, ring->batch,
+                                          ring->n_kv_heads, ring->head_dim, ring->sink, ring->window, h, err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+wm_status wm_ring_rollback(const wm_ring *ring, const int64_t *new_len, void *stream) {
+    if (!ring_ok(ring) || !new_len || !aligned(new_len, 8)) return WM_ERR_INVALID_ARG;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    return launch_status(launch_ring_rollback(ring->pos_tag, ring->n_seen, ring->batch,
+                                              ring->sink + ring->window, new_len, err,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
+                       int32_t head_dim, void *out, float *lse_out, void *stream) {
+    if (!o_parts || !lse_parts || !out || n_parts <= 0 || rows < 0 || head_dim <= 0 || rows > INT32_MAX)
+        return WM_ERR_INVALID_ARG;
+    if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(out, 2) || (lse_out && !aligned(lse_out, 4)))
+        return WM_ERR_INVALID_ARG;
+    if ((size_t)n_parts * sizeof(float) > 200 * 1024) return WM_ERR_UNSUPPORTED;
+    return launch_status(launch_lse_merge(o_parts, lse_parts, n_parts, rows, head_dim, out, lse_out, nullptr,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+// Shared tail of the two attention entry points: plan, check the workspace,
+// launch the attention kernel and (if split) the merge.
+static wm_status run_attention(AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv, int64_t max_keys,
+                               int32_t n_split, void *out, float *lse, void *ws, size_t ws_bytes,
+                               cudaStream_t st) {
+    const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, max_keys, n_split);
+    const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
+    p.n_split = pl.n_split;
+    p.keys_per_split = pl.keys_per_split;
+    p.out = out;
+    p.lse = lse;
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
+    if (pl.n_split > 1) {
+        const size_t need = partial_bytes(rows_total, pl.n_split, p.head_dim);
+        if (!ws || ws_bytes < need || !aligned(ws, 256)) return WM_ERR_WORKSPACE;
+        const size_t o = (size_t)rows_total * pl.n_split * p.head_dim * sizeof(float);
+        p.o_part = static_cast<float *>(ws);
+        p.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + ((o + 255) & ~(size_t)255));
+    }
+    const int m_tiles = (p.rows + 15) / 16;
+    cudaError_t e = launch_attn_any(mk, mv, p, m_tiles, st);
+    if (e != cudaSuccess) return WM_ERR_CUDA;
+    if (pl.n_split > 1) {
+        e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, st);
+        if (e != cudaSuccess) return WM_ERR_CUDA;
+    }
+    return WM_OK;
+}
+
+wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
+                        void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!ring_ok(ring) || !q || !out || n_q_heads <= 0 || n_split < 0 || !std::isfinite(scale))
+        return WM_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return WM_ERR_INVALID_ARG;
+    if (n_q_heads % ring->n_kv_heads) return WM_ERR_INVALID_ARG;
+    const int group = n_q_heads / ring->n_kv_heads;
+    if (group > kMaxRows) return WM_ERR_UNSUPPORTED;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    const int n_slots = ring->sink + ring->window;
+    CUtensorMap mk, mv;
+    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch) ||
+        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch))
+        return WM_ERR_CUDA;
+    AttnParams p;
+    std::memset(&p, 0, sizeof p);
+    p.source = KEYS_RING;
+    p.batch = ring->batch;
+    p.n_kv_heads = ring->n_kv_heads;
+    p.head_dim = ring->head_dim;
+    p.pos_tag = ring->pos_tag;
+    p.n_seen = ring->n_seen;
+    p.n_slots = n_slots;
+    p.sink = ring->sink;
+    p.window = ring->window;
+    p.capacity = n_slots;
+    p.q = q;
+    p.n_q = 1;
+    p.n_q_heads = n_q_heads;
+    p.group = group;
+    p.rows = group;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.err = err;
+    return run_attention(p, mk, mv, n_slots, n_split, out, lse, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_q_heads, float scale,
+                         int32_t n_split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    const wm_status ks = kv_check(kv, true);
+    if (ks != WM_OK) return ks;
+    if (!q || !out || n_q <= 0 || n_q_heads <= 0 || n_split < 0 || !std::isfinite(scale))
+        return WM_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return WM_ERR_INVALID_ARG;
+    if (n_q_heads % kv->n_kv_heads) return WM_ERR_INVALID_ARG;
+    const int group = n_q_heads / kv->n_kv_heads;
+    if ((int64_t)group * n_q > kMaxRows) return WM_ERR_UNSUPPORTED;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    const bool paged = kv->block_table != nullptr;
+    const int64_t capacity = paged ? (int64_t)kv->max_pages * kv->page_size : kv->n_cap;
+    CUtensorMap mk, mv;
+    const int64_t inner = paged ? kv->page_size : kv->n_cap;
+    const int64_t outer = paged ? kv->n_pages : kv->batch;
+    if (!encode_kv_map(&mk, kv->k, kv->head_dim, inner, kv->n_kv_heads, outer) ||
+        !encode_kv_map(&mv, kv->v, kv->head_dim, inner, kv->n_kv_heads, outer))
+        return WM_ERR_CUDA;
+    AttnParams p;
+    std::memset(&p, 0, sizeof p);
+    p.source = paged ? KEYS_PAGED : KEYS_CONTIG;
+    p.batch = kv->batch;
+    p.n_kv_heads = kv->n_kv_heads;
+    p.head_dim = kv->head_dim;
+    p.seq_lens = kv->seq_lens;
+    p.block_table = kv->block_table;
+    p.capacity = capacity;
+    p.n_pages = kv->n_pages;
+    p.page_size = kv->page_size;
+    p.max_pages = kv->max_pages;
+    p.q = q;
+    p.n_q = n_q;
+    p.n_q_heads = n_q_heads;
+    p.group = group;
+    p.rows = group * n_q;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.err = err;
+    return run_attention(p, mk, mv, capacity, n_split, out, lse, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

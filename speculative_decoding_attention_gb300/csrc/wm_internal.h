@@ -1,0 +1,99 @@
+// wm_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace wm {
+
+// Key source of an attention launch.
+enum KeySource : int32_t {
+    KEYS_CONTIG = 0,  // verify over a contiguous cache [B][Hkv][n_cap][D]
+    KEYS_PAGED = 1,   // verify over a paged cache [pages][Hkv][page][D]
+    KEYS_RING = 2,    // draft over the ring [B][Hkv][S+W][D] with slot tags
+};
+
+// Keys handled per pipeline stage by the attention kernel (all head dims).
+constexpr int kKeyTile = 64;
+// Shared-memory bytes given to KV staging (stages = this / stage bytes).
+constexpr int kStagingBytes = 128 * 1024;
+// Consumer warps + one producer warp.
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Polls of an mbarrier before a wait is declared lost.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+struct AttnParams {
+    int32_t source;       // KeySource
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    // verify (contiguous / paged)
+    const int64_t *seq_lens;
+    const int32_t *block_table;
+    int64_t capacity;     // positions a sequence can hold (n_cap or max_pages * page_size)
+    int64_t n_pages;
+    int32_t page_size;
+    int32_t max_pages;
+    // draft (ring)
+    const int32_t *pos_tag;
+    const int64_t *n_seen;
+    int32_t n_slots;
+    int32_t sink;
+    int32_t window;
+    // queries: rows of one KV head = n_q positions x group heads, row r = i * group + hh
+    const void *q;        // verify [B][n_q][Hq][D]; draft [B][Hq][D]
+    int32_t n_q;
+    int32_t n_q_heads;
+    int32_t group;
+    int32_t rows;
+    float scale_log2;     // scale * log2(e)
+    // split
+    int32_t n_split;
+    int32_t keys_per_split;  // multiple of kKeyTile
+    // outputs
+    void *out;            // bf16, same layout as q
+    float *lse;           // [B][n_q][Hq] or NULL
+    float *o_part;        // [B*n_q*Hq][n_split][D] fp32, NULL when unsplit
+    float *lse_part;      // [B*n_q*Hq][n_split]
+    int32_t *err;         // device error word
+};
+
+// Launch the attention kernel for head dim D (defined in attn_d<D>.cu).
+cudaError_t launch_attn_d64(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                            int m_tiles, cudaStream_t stream);
+cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                             int m_tiles, cudaStream_t stream);
+cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                             int m_tiles, cudaStream_t stream);
+
+// Ring and merge kernels (ring.cu, merge.cu).
+cudaError_t launch_ring_append(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
+                               int n_kv_heads, int head_dim, int sink, int window,
+                               const void *k_new, const void *v_new, int32_t *err,
+                               cudaStream_t stream);
+
+struct HistSource {
+    const void *k;
+    const void *v;
+    const int64_t *lens;
+    const int32_t *block_table;
+    int64_t n_cap;
+    int64_t n_pages;
+    int32_t page_size;
+    int32_t max_pages;
+};
+
+cudaError_t launch_ring_fill(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
+                             int n_kv_heads, int head_dim, int sink, int window,
+                             const HistSource &hist, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_ring_rollback(int32_t *tag, int64_t *n_seen, int batch, int n_slots,
+                                 const int64_t *new_len, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n_parts,
+                             int64_t rows, int head_dim, void *out, float *lse_out,
+                             const int32_t *row_map, cudaStream_t stream);
+
+}  // namespace wm

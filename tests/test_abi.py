@@ -1,0 +1,127 @@
+"""The C ABI library (no GPU needed): it loads, exports every declared symbol,
+and rejects invalid arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_attention_gb300 import build as wm_build
+from speculative_decoding_attention_gb300 import wm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wm_api.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wm_build.build()
+    return wm.load()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wm_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(declared_functions()) == set(wm.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert wm.status_string(wm.WM_OK) == "ok"
+    assert "workspace" in wm.status_string(wm.WM_ERR_WORKSPACE)
+    assert lib.wm_version() >= 100
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    P = ctypes.c_void_p
+    assert lib.wm_ring_append(None, P(16), P(16), None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_ring_fill(None, None, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_ring_rollback(None, None, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_draft_attn(None, P(16), 8, 1.0, 0, P(16), None, None, 0, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_verify_attn(None, P(16), 2, 8, 1.0, 0, P(16), None, None, 0, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_lse_merge(None, None, 4, 10, 128, None, None, None) == wm.WM_ERR_INVALID_ARG
+
+
+def _ring(**over):
+    r = wm._Ring()
+    r.k, r.v, r.pos_tag, r.n_seen = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    r.batch, r.n_kv_heads, r.head_dim, r.sink, r.window = 1, 2, 128, 4, 256
+    for k, v in over.items():
+        setattr(r, k, v)
+    return r
+
+
+def _kv(**over):
+    s = wm._KV()
+    s.k, s.v, s.seq_lens, s.block_table = 1 << 20, 2 << 20, 3 << 20, None
+    s.n_cap, s.n_pages, s.page_size, s.max_pages = 4096, 0, 0, 0
+    s.batch, s.n_kv_heads, s.head_dim = 1, 2, 128
+    for k, v in over.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(head_dim=96), wm.WM_ERR_INVALID_ARG),
+    (dict(window=0), wm.WM_ERR_INVALID_ARG),
+    (dict(sink=-1), wm.WM_ERR_INVALID_ARG),
+    (dict(k=(1 << 20) + 2), wm.WM_ERR_INVALID_ARG),
+    (dict(batch=0), wm.WM_ERR_INVALID_ARG),
+])
+def test_bad_ring_shapes(lib, over, status):
+    r = _ring(**over)
+    P = ctypes.c_void_p
+    assert lib.wm_draft_attn(ctypes.byref(r), P(1 << 24), 8, 1.0, 0, P(1 << 25), None, None, 0,
+                             None) == status
+
+
+def test_bad_draft_heads(lib):
+    r = _ring()
+    P = ctypes.c_void_p
+    # 7 query heads do not divide over 2 KV heads
+    assert lib.wm_draft_attn(ctypes.byref(r), P(1 << 24), 7, 1.0, 0, P(1 << 25), None, None, 0,
+                             None) == wm.WM_ERR_INVALID_ARG
+    # non-finite scale
+    assert lib.wm_draft_attn(ctypes.byref(r), P(1 << 24), 8, float("nan"), 0, P(1 << 25), None, None,
+                             0, None) == wm.WM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over,n_q,hq,status", [
+    (dict(head_dim=80), 2, 8, wm.WM_ERR_UNSUPPORTED),
+    (dict(), 9, 64, wm.WM_ERR_UNSUPPORTED),              # 9 positions x 32 grouped heads > 64 rows
+    (dict(), 2, 9, wm.WM_ERR_INVALID_ARG),               # 9 query heads over 2 KV heads
+    (dict(n_cap=0), 2, 8, wm.WM_ERR_INVALID_ARG),
+    (dict(block_table=5 << 20, page_size=16, max_pages=4, n_pages=8), 2, 8, wm.WM_ERR_UNSUPPORTED),
+    (dict(block_table=5 << 20, page_size=64, max_pages=0, n_pages=8), 2, 8, wm.WM_ERR_INVALID_ARG),
+])
+def test_bad_verify_shapes(lib, over, n_q, hq, status):
+    s = _kv(**over)
+    P = ctypes.c_void_p
+    assert lib.wm_verify_attn(ctypes.byref(s), P(1 << 24), n_q, hq, 1.0, 0, P(1 << 25), None, None, 0,
+                              None) == status
+
+
+def test_workspace_size_with_explicit_splits(lib):
+    # Explicit split counts need no device query.
+    assert wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, 1) == 0
+    rows, ns, D = 1 * 4 * 16, 8, 256
+    o = rows * ns * D * 4
+    assert wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, ns) == \
+        ((o + 255) // 256) * 256 + rows * ns * 4
+    assert wm.plan_splits(wm.WM_OP_DRAFT, 1, 2, 16, 1, 256, 4100, 1000) == 65  # capped at one tile each
+    with pytest.raises(wm.WmError):
+        wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 96, 1 << 20, 0)
+
+
+def test_library_has_no_torch_dependency(lib):
+    # The C ABI is plain pointers and sizes: the shared object links no torch.
+    data = open(wm.library_path(), "rb").read()
+    assert b"libtorch" not in data and b"libc10" not in data

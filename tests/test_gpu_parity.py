@@ -1,0 +1,202 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Sizes are small enough for the oracle to evaluate every row in seconds but
+span several 64-key tiles and splits, with ragged tails.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_attention_gb300 import inputs, wm, workloads
+
+from parity import assert_close, gpu, oracle_kv
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_bf16(shape, gen, device, std=1.0):
+    return (torch.randn(shape, generator=gen, device=device) * std).to(torch.bfloat16)
+
+
+def run_step(w, context, depth, dev, n_split=0, check_verify=True):
+    """Ring fill + d draft steps + verify through the library; compare each with the oracle."""
+    inp = inputs.make_inputs(w, depth=depth, device=dev, context=context)
+    kv = wm.KVCache(inp.k, inp.v, inp.seq_lens, inp.block_table)
+    ring = wm.Ring.create(w.batch, w.n_kv_heads, w.head_dim, w.sink, w.window, dev)
+    wm.ring_fill(ring, kv)
+    hist = oracle_kv(inp.k, inp.v, inp.block_table)
+    for j in range(depth):
+        wm.ring_append(ring, inp.k_new[j], inp.v_new[j])
+        out, lse = wm.draft_attn(ring, inp.q_draft[j], w.scale, n_split=n_split)
+        pos = [n + j for n in inp.seq_lens_host]
+        ref, ref_lse = oracle.draft(hist, inp.q_draft[j].cpu(), pos, w.sink, w.window, w.scale)
+        assert_close(f"{w.name} draft step {j}", out, lse, ref, ref_lse)
+    if check_verify:
+        out, lse = wm.verify_attn(kv, inp.q_verify, w.scale, n_split=n_split)
+        ref, ref_lse = oracle.verify(hist, inp.q_verify.cpu(), inp.seq_lens_host, w.scale)
+        assert_close(f"{w.name} verify", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
+@pytest.mark.parametrize("name,context", [
+    ("tiny_4k", 4096), ("gqa8_128k", 3000), ("hybrid_1m_d256", 5000),
+    ("paged_ragged_b8", 1500), ("nope_1m_b2", 9000)])
+def test_workloads_reduced_context(name, context):
+    run_step(workloads.get(name), context, workloads.get(name).max_depth, gpu())
+
+
+@pytest.mark.parametrize("n_split", [1, 3, 64])
+def test_forced_split_counts(n_split):
+    run_step(workloads.get("tiny_4k"), 4096, 1, gpu(), n_split=n_split)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G,T", [(1, 1), (4, 3), (8, 2), (16, 4)])
+def test_verify_shapes(D, G, T):
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(100 + D + 7 * G + T)
+    B, Hkv = 2, 2
+    Hq = G * Hkv
+    lens = [1000 + 37 * D // 64, 613]
+    cap = 1200
+    k = rand_bf16((B, Hkv, cap, D), gen, dev)
+    v = rand_bf16((B, Hkv, cap, D), gen, dev)
+    q = rand_bf16((B, T, Hq, D), gen, dev, 1.0)
+    seq = torch.tensor(lens, dtype=torch.int64, device=dev)
+    kv = wm.KVCache(k, v, seq)
+    s = 1 / math.sqrt(D)
+    for ns in (0, 1, 5):
+        out, lse = wm.verify_attn(kv, q, s, n_split=ns)
+        ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), lens, s)
+        assert_close(f"verify D={D} G={G} T={T} ns={ns}", out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("S,W", [(0, 1), (0, 100), (4, 60), (16, 200), (3, 1)])
+def test_draft_ring_wraps(D, S, W):
+    """Appends past several wraps of a small window; every step checked."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(200 + D + S + W)
+    B, Hkv, G = 2, 2, 4
+    n_pos = 3 * (S + W) + 7
+    hk = rand_bf16((B, Hkv, n_pos, D), gen, dev)
+    hv = rand_bf16((B, Hkv, n_pos, D), gen, dev)
+    hist = oracle_kv(hk, hv)
+    ring = wm.Ring.create(B, Hkv, D, S, W, dev)
+    q = rand_bf16((n_pos, B, Hkv * G, D), gen, dev, 1 / math.sqrt(D))
+    check_at = sorted({0, 1, S, S + W - 1, S + W, S + W + 1, n_pos // 2, n_pos - 1} & set(range(n_pos)))
+    for p in range(n_pos):
+        wm.ring_append(ring, hk[:, :, p].contiguous(), hv[:, :, p].contiguous())
+        if p in check_at:
+            out, lse = wm.draft_attn(ring, q[p], 1.0)
+            ref, ref_lse = oracle.draft(hist, q[p].cpu(), [p] * B, S, W, 1.0)
+            assert_close(f"draft D={D} S={S} W={W} p={p}", out, lse, ref, ref_lse)
+
+
+def test_draft_with_window_covering_everything_equals_verify():
+    """S + W >= p + 1: windowed draft equals full causal attention (single query)."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(300)
+    B, Hkv, D, G = 1, 2, 128, 8
+    n = 700
+    hk, hv = rand_bf16((B, Hkv, n, D), gen, dev), rand_bf16((B, Hkv, n, D), gen, dev)
+    ring = wm.Ring.create(B, Hkv, D, 4, 1000, dev)
+    wm.ring_fill(ring, wm.KVCache(hk, hv, torch.tensor([n], device=dev)))
+    q = rand_bf16((B, Hkv * G, D), gen, dev, 0.1)
+    d_out, d_lse = wm.draft_attn(ring, q, 1.0)
+    v_out, v_lse = wm.verify_attn(wm.KVCache(hk, hv, torch.tensor([n], device=dev)), q[:, None], 1.0)
+    ref, ref_lse = oracle.verify(oracle_kv(hk, hv), q[:, None].cpu(), [n], 1.0)
+    assert_close("draft==full", d_out, d_lse, ref, ref_lse)
+    assert_close("verify T=1", v_out, v_lse, ref, ref_lse)
+
+
+def test_ring_slot_rotation_invariance():
+    """Permuting ring slots together with their tags leaves the draft output unchanged."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(301)
+    B, Hkv, D, G, S, W = 2, 2, 128, 4, 4, 300
+    n = 1000
+    hk, hv = rand_bf16((B, Hkv, n, D), gen, dev), rand_bf16((B, Hkv, n, D), gen, dev)
+    ring = wm.Ring.create(B, Hkv, D, S, W, dev)
+    wm.ring_fill(ring, wm.KVCache(hk, hv, torch.full((B,), n, dtype=torch.int64, device=dev)))
+    q = rand_bf16((B, Hkv * G, D), gen, dev, 0.1)
+    a_out, a_lse = wm.draft_attn(ring, q, 1.0)
+    perm = torch.randperm(S + W, generator=gen, device=dev)
+    rot = wm.Ring(ring.k[:, :, perm].contiguous(), ring.v[:, :, perm].contiguous(),
+                  ring.pos_tag[:, perm].contiguous(), ring.n_seen.clone(), S, W)
+    b_out, b_lse = wm.draft_attn(rot, q, 1.0)
+    ref, ref_lse = oracle.draft(oracle_kv(hk, hv), q.cpu(), [n - 1] * B, S, W, 1.0)
+    assert_close("ring", a_out, a_lse, ref, ref_lse)
+    assert_close("rotated ring", b_out, b_lse, ref, ref_lse)
+
+
+def test_empty_and_degenerate_cases():
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(302)
+    B, Hkv, D, G, T = 3, 1, 64, 2, 3
+    cap = 200
+    k, v = rand_bf16((B, Hkv, cap, D), gen, dev), rand_bf16((B, Hkv, cap, D), gen, dev)
+    # seq_len 0 (no keys at all), seq_len 2 < T (first query has no key), seq_len 1
+    lens = [0, 2, 1]
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev)
+    out, lse = wm.verify_attn(wm.KVCache(k, v, torch.tensor(lens, device=dev)), q, 0.3, n_split=2)
+    ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), lens, 0.3)
+    assert_close("degenerate verify", out, lse, ref, ref_lse)
+    # empty ring (nothing appended): no key, out 0 / lse -inf
+    ring = wm.Ring.create(1, 1, D, 4, 16, dev)
+    q1 = rand_bf16((1, G, D), gen, dev)
+    out, lse = wm.draft_attn(ring, q1, 1.0)
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_stale_bytes_beyond_length_never_leak():
+    """NaN/Inf bit patterns in cache rows past seq_len and in never-written ring
+    slots must not reach the output (masked keys get zero weight and zeroed V)."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(303)
+    B, Hkv, D, G, T = 1, 2, 128, 4, 2
+    cap, n = 640, 517
+    k, v = rand_bf16((B, Hkv, cap, D), gen, dev), rand_bf16((B, Hkv, cap, D), gen, dev)
+    k[:, :, n:] = float("nan")
+    v[:, :, n:] = float("inf")
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev, 0.1)
+    out, lse = wm.verify_attn(wm.KVCache(k, v, torch.tensor([n], device=dev)), q, 1.0)
+    ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), [n], 1.0)
+    assert_close("verify with NaN tail", out, lse, ref, ref_lse)
+    ring = wm.Ring.create(B, Hkv, D, 4, 200, dev)
+    ring.k.fill_(float("nan"))
+    ring.v.fill_(float("nan"))
+    for p in range(50):
+        wm.ring_append(ring, k[:, :, p].contiguous(), v[:, :, p].contiguous())
+    q1 = rand_bf16((B, Hkv * G, D), gen, dev, 0.1)
+    out, lse = wm.draft_attn(ring, q1, 1.0)
+    ref, ref_lse = oracle.draft(oracle_kv(k, v), q1.cpu(), [49], 4, 200, 1.0)
+    assert_close("draft over partly written ring", out, lse, ref, ref_lse)
+
+
+def test_paged_verify_matches_contiguous_oracle():
+    dev = gpu()
+    w = workloads.get("paged_ragged_b8")
+    inp = inputs.make_inputs(w, depth=2, device=dev, context=3000, seed_offset=3)
+    kv = wm.KVCache(inp.k, inp.v, inp.seq_lens, inp.block_table)
+    for ns in (0, 1, 7):
+        out, lse = wm.verify_attn(kv, inp.q_verify, w.scale, n_split=ns)
+        ref, ref_lse = oracle.verify(oracle_kv(inp.k, inp.v, inp.block_table), inp.q_verify.cpu(),
+                                     inp.seq_lens_host, w.scale)
+        assert_close(f"paged ns={ns}", out, lse, ref, ref_lse)
+
+
+def test_lse_merge_kernel_matches_oracle():
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(304)
+    rows, parts, D = 37, 11, 256
+    o = torch.randn((rows, parts, D), generator=gen, device=dev)
+    ls = torch.randn((rows, parts), generator=gen, device=dev) * 5
+    ls[3, :] = -float("inf")           # a row with only empty parts
+    ls[5, ::2] = -float("inf")         # some empty parts
+    out, lse = wm.lse_merge(o, ls)
+    ref, ref_lse = oracle.lse_merge(o.double().cpu().numpy(), ls.double().cpu().numpy())
+    assert_close("lse_merge", out, lse, ref, ref_lse)
