@@ -188,6 +188,36 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
 wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
                        int32_t head_dim, void *out, float *lse_out, void *stream);
 
+/*
+ * Draft attention for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart: this is a deployment convenience.  Some
+ * callers have no way to obtain the workspace that wm_draft_attn needs --
+ * runtimes that reserve all device memory at start-up and refuse any later
+ * allocation, plugins hosted by a framework that owns the GPU allocator and
+ * hands them no scratch, and tight decode loops where a cudaMalloc would
+ * synchronise the device.  This entry point computes exactly what
+ * wm_draft_attn computes (same arguments minus the workspace), keeping the
+ * split partials in a scratch array built into the library instead.
+ *
+ *   - The scratch is WM_STATIC_SCRATCH_BYTES per device and stays allocated on
+ *     every GPU that loads the library until the process exits.
+ *   - If the split partials of a call would need more than that (see
+ *     wm_workspace_size with WM_OP_DRAFT), the call returns WM_ERR_WORKSPACE and
+ *     enqueues nothing; pass a smaller n_split or use wm_draft_attn.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array and leaves its partials in
+ *     it.  Nothing in it needs to start at zero.  Calls whose kernels can
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race on the array: order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree.
+ */
+#define WM_STATIC_SCRATCH_BYTES (8u << 20)
+wm_status wm_draft_attn_static(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale,
+                               int32_t n_split, void *out, float *lse, void *stream);
+
 /* Operations for wm_workspace_size / wm_plan_splits. */
 #define WM_OP_DRAFT 0
 #define WM_OP_VERIFY 1

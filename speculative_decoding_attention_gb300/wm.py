@@ -22,7 +22,8 @@ DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait tim
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
-            "wm_status_string", "wm_version")
+            "wm_status_string", "wm_version", "wm_draft_attn_static")
+STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
 
 _lib = None
 _lock = threading.Lock()
@@ -67,6 +68,7 @@ def load() -> ctypes.CDLL:
         lib.wm_ring_rollback.argtypes = [P, P, P]
         lib.wm_draft_attn.argtypes = [P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_verify_attn.argtypes = [P, P, I32, I32, F, I32, P, P, P, ctypes.c_size_t, P]
+        lib.wm_draft_attn_static.argtypes = [P, P, I32, F, I32, P, P, P]
         lib.wm_lse_merge.argtypes = [P, P, I32, I64, I32, P, P, P]
         lib.wm_plan_splits.argtypes = [I32, I32, I32, I32, I32, I32, I64, I32]
         lib.wm_plan_splits.restype = I32
@@ -76,7 +78,7 @@ def load() -> ctypes.CDLL:
         lib.wm_status_string.argtypes = [I32]
         lib.wm_status_string.restype = ctypes.c_char_p
         lib.wm_version.restype = I32
-        for name in ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn",
+        for name in ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_draft_attn_static",
                      "wm_verify_attn", "wm_lse_merge", "wm_get_device_error"):
             getattr(lib, name).restype = I32
         _lib = lib
@@ -262,6 +264,26 @@ def draft_attn(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=
     _check(load().wm_draft_attn(ctypes.byref(r), _dev(q, torch.bfloat16, "q"), Hq, float(scale), n_split,
                                 _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"), ws,
                                 ws_bytes, _stream(stream)), "wm_draft_attn")
+    return out, lse
+
+
+def draft_attn_static(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=None, lse=None,
+                      stream=None):
+    """Draft attention for callers that cannot allocate device memory: the
+    split partials live in a fixed scratch array inside the library
+    (STATIC_SCRATCH_BYTES per device) instead of a workspace, so this call
+    allocates nothing beyond the outputs it is not given.  Calls that can
+    overlap on the GPU share that array and race; keep them on one stream."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    r = ring.c()
+    _check(load().wm_draft_attn_static(ctypes.byref(r), _dev(q, torch.bfloat16, "q"), Hq, float(scale),
+                                       n_split, _dev(out, torch.bfloat16, "out"),
+                                       _dev(lse, torch.float32, "lse"), _stream(stream)),
+           "wm_draft_attn_static")
     return out, lse
 
 
