@@ -485,14 +485,21 @@ def pick_fraction(w, depth, inp_host, budget_s):
     return max(probe, frac)
 
 
-def cpu_baseline(st: Step, args) -> dict:
+def cpu_baseline(st: Step, args, min_seconds: float = 10.0) -> dict:
+    """The oracle timed on repeated bounded samples until about ``min_seconds``
+    of CPU work have run; reported per whole step."""
     import oracle
 
     inp_host = host_inputs(st.inp)
-    frac = pick_fraction(st.w, st.d, inp_host, budget_s=8.0)
-    secs, per_step, desc = oracle_sample(st.w, st.d, inp_host, frac)
-    return {"value": round(per_step * 1e6, 1), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": desc, "sample_seconds": round(secs, 2)}
+    frac = pick_fraction(st.w, st.d, inp_host, budget_s=min_seconds / 2)
+    total, per_steps, desc = 0.0, [], ""
+    while total < min_seconds:
+        secs, per_step, desc = oracle_sample(st.w, st.d, inp_host, frac)
+        total += secs
+        per_steps.append(per_step)
+    return {"value": round(1e6 * sum(per_steps) / len(per_steps), 1), "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(per_steps)} x ({desc})", "sample_seconds": round(total, 2)}
 
 
 def reference_arm(args, rank, world, local):

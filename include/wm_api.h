@@ -184,6 +184,8 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
  *   lse_parts [rows][n_parts] fp32 natural log; -inf marks an empty part
  *   out       [rows][head_dim] bf16;  lse_out [rows] fp32, may be NULL.
  * A row whose parts are all empty gets out = 0, lse = -inf.
+ * head_dim must be a multiple of 4 (WM_ERR_UNSUPPORTED otherwise); o_parts must
+ * be 16-byte and out 8-byte aligned (WM_ERR_INVALID_ARG otherwise).
  */
 wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
                        int32_t head_dim, void *out, float *lse_out, void *stream);

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "launch.h"
 #include "ptx.cuh"
 #include "wm_internal.h"
 #include "../../include/wm_api.h"
@@ -102,6 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = unit / p.n_kv_heads;
     const int kvh = unit - b * p.n_kv_heads;
     const int split = blockIdx.x;
+
+    pdl_wait();  // every global read below may depend on the previous kernel
+    pdl_launch_dependents();
 
     // ---- keys of this split, and the position of query 0
     int64_t n_keys, qpos0;
@@ -483,8 +487,7 @@ cudaError_t launch_attn_mt(const CUtensorMap &k, const CUtensorMap &v, const Att
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    attn_kernel<D, MT><<<grid, kThreads, smem, stream>>>(k, v, p);
-    return cudaGetLastError();
+    return launch_pdl(attn_kernel<D, MT>, grid, dim3(kThreads), smem, stream, k, v, p);
 }
 
 template <int D>

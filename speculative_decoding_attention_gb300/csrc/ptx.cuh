@@ -143,3 +143,17 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk16) {
 }
 
 }  // namespace wm
+
+namespace wm {
+
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when this kernel
+// was launched without the programmatic-serialisation attribute) ...
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ... and let the next kernel in the stream start launching now.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace wm

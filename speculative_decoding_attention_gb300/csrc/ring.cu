@@ -8,6 +8,8 @@
 // compact ring buffer).
 #include <cuda_bf16.h>
 
+#include "launch.h"
+#include "ptx.cuh"
 #include "wm_internal.h"
 #include "../../include/wm_api.h"
 
@@ -34,6 +36,8 @@ __device__ __forceinline__ int64_t latest_in_slot(int64_t s, int64_t n, int sink
 __global__ void ring_append_kernel(uint4 *rk, uint4 *rv, int32_t *tag, int64_t *n_seen, int n_kv_heads,
                                    int head_dim, int sink, int window, const uint4 *kn,
                                    const uint4 *vn, int32_t *err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.x;
     const int n_slots = sink + window;
     const int64_t p = n_seen[b];
@@ -61,6 +65,8 @@ constexpr int kFillSlots = 32;  // slots per block in the bulk fill
 
 __global__ void ring_fill_kernel(uint4 *rk, uint4 *rv, int32_t *tag, int64_t *n_seen, int n_kv_heads,
                                  int head_dim, int sink, int window, HistSource hist, int32_t *err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int unit = blockIdx.y;
     const int b = unit / n_kv_heads, h = unit - (unit / n_kv_heads) * n_kv_heads;
     const int n_slots = sink + window;
@@ -103,19 +109,26 @@ __global__ void ring_fill_kernel(uint4 *rk, uint4 *rv, int32_t *tag, int64_t *n_
     }
 }
 
+constexpr int kRollbackThreads = 256;
+
+// One thread per slot; block (0, b) also lowers n_seen[b].  No block reads
+// n_seen, so the update cannot race with the tag clearing.
 __global__ void ring_rollback_kernel(int32_t *tag, int64_t *n_seen, int n_slots, const int64_t *new_len,
                                      int32_t *err) {
-    const int b = blockIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int b = blockIdx.y;
     const int64_t nl = new_len[b];
     if (nl < 0) {
-        if (threadIdx.x == 0) report(err, WM_DEVERR_BAD_LENGTH);
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(err, WM_DEVERR_BAD_LENGTH);
         return;
     }
-    for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+    const int s = blockIdx.x * kRollbackThreads + threadIdx.x;
+    if (s < n_slots) {
         int32_t *t = tag + (int64_t)b * n_slots + s;
         if (*t >= nl) *t = -1;
     }
-    if (threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int64_t seen = n_seen[b];
         n_seen[b] = seen < nl ? seen : nl;
     }
@@ -126,10 +139,9 @@ __global__ void ring_rollback_kernel(int32_t *tag, int64_t *n_seen, int n_slots,
 cudaError_t launch_ring_append(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
                                int n_kv_heads, int head_dim, int sink, int window, const void *k_new,
                                const void *v_new, int32_t *err, cudaStream_t stream) {
-    ring_append_kernel<<<batch, 128, 0, stream>>>(
-        static_cast<uint4 *>(rk), static_cast<uint4 *>(rv), tag, n_seen, n_kv_heads, head_dim, sink,
-        window, static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), err);
-    return cudaGetLastError();
+    return launch_pdl(ring_append_kernel, dim3(batch), dim3(128), 0, stream, static_cast<uint4 *>(rk),
+                      static_cast<uint4 *>(rv), tag, n_seen, n_kv_heads, head_dim, sink, window,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), err);
 }
 
 cudaError_t launch_ring_fill(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
@@ -137,15 +149,15 @@ cudaError_t launch_ring_fill(void *rk, void *rv, int32_t *tag, int64_t *n_seen, 
                              int32_t *err, cudaStream_t stream) {
     const int n_slots = sink + window;
     const dim3 grid((n_slots + kFillSlots - 1) / kFillSlots, batch * n_kv_heads);
-    ring_fill_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(rk), static_cast<uint4 *>(rv), tag,
-                                               n_seen, n_kv_heads, head_dim, sink, window, hist, err);
-    return cudaGetLastError();
+    return launch_pdl(ring_fill_kernel, grid, dim3(256), 0, stream, static_cast<uint4 *>(rk),
+                      static_cast<uint4 *>(rv), tag, n_seen, n_kv_heads, head_dim, sink, window, hist, err);
 }
 
 cudaError_t launch_ring_rollback(int32_t *tag, int64_t *n_seen, int batch, int n_slots,
                                  const int64_t *new_len, int32_t *err, cudaStream_t stream) {
-    ring_rollback_kernel<<<batch, 256, 0, stream>>>(tag, n_seen, n_slots, new_len, err);
-    return cudaGetLastError();
+    const dim3 grid((n_slots + kRollbackThreads - 1) / kRollbackThreads, batch);
+    return launch_pdl(ring_rollback_kernel, grid, dim3(kRollbackThreads), 0, stream, tag, n_seen, n_slots,
+                      new_len, err);
 }
 
 }  // namespace wm

@@ -240,9 +240,9 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
                        int32_t head_dim, void *out, float *lse_out, void *stream) {
     if (!o_parts || !lse_parts || !out || n_parts <= 0 || rows < 0 || head_dim <= 0 || rows > INT32_MAX)
         return WM_ERR_INVALID_ARG;
-    if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(out, 2) || (lse_out && !aligned(lse_out, 4)))
+    if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 8) || (lse_out && !aligned(lse_out, 4)))
         return WM_ERR_INVALID_ARG;
-    if ((size_t)n_parts * sizeof(float) > 200 * 1024) return WM_ERR_UNSUPPORTED;
+    if (head_dim % 4) return WM_ERR_UNSUPPORTED;
     return launch_status(launch_lse_merge(o_parts, lse_parts, n_parts, rows, head_dim, out, lse_out, nullptr,
                                           static_cast<cudaStream_t>(stream)));
 }

@@ -1,0 +1,57 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+Each workload's step state is built exactly as the bench builds it (ring fill,
+and for the NoPE workload 20,000 single appends that wrap the window), then:
+every draft row of every draft step is compared with the oracle; the verify is
+compared on a sample of rows the oracle evaluates one by one (first, last and
+evenly spaced rows of the [batch, T, Hq] space); the ring's tags are compared
+with the StreamingLLM cache model.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.ring_model import held_after
+
+from parity import assert_close, gpu, oracle_kv
+
+pytestmark = pytest.mark.gpu
+
+N_VERIFY_ROWS = 12
+
+
+@pytest.mark.parametrize("name", ["tiny_4k", "gqa8_128k", "hybrid_1m_d256", "paged_ragged_b8", "nope_1m_b2"])
+def test_full_size_step(name):
+    dev = gpu()
+    import bench
+    from speculative_decoding_attention_gb300 import wm, workloads
+
+    w = workloads.get(name)
+    depth = workloads.BENCH_DEPTH if name == workloads.BENCH_WORKLOAD else w.max_depth
+    st = bench.Step(w, depth, dev)
+    inp = st.inp
+    torch.cuda.synchronize()
+    assert wm.get_device_error() == 0
+    # ring after fill (+ appends): exactly the sinks and the last W positions
+    tags = st.ring.pos_tag.cpu()
+    for b, n in enumerate(inp.seq_lens_host):
+        t = tags[b]
+        assert sorted(int(x) for x in t[t >= 0]) == held_after(w.sink, w.window, n)
+
+    st.run()
+    torch.cuda.synchronize()
+    assert wm.get_device_error() == 0
+    hist = oracle_kv(inp.k, inp.v, inp.block_table)
+    for j in range(depth):
+        pos = [n + j for n in inp.seq_lens_host]
+        ref, ref_lse = oracle.draft(hist, inp.q_draft[j].cpu(), pos, w.sink, w.window, w.scale)
+        assert_close(f"{name} draft step {j}", st.d_out[j], st.d_lse[j], ref, ref_lse)
+
+    T, Hq, D = st.T, w.n_q_heads, w.head_dim
+    total = w.batch * T * Hq
+    rows = sorted({0, total - 1, *np.linspace(0, total - 1, N_VERIFY_ROWS).astype(int).tolist()})
+    ref, ref_lse = oracle.verify(hist, inp.q_verify.cpu(), inp.seq_lens_host, w.scale, rows=rows)
+    got = st.v_out.reshape(total, D)[rows]
+    got_lse = st.v_lse.reshape(total)[rows]
+    assert_close(f"{name} verify (sampled rows {rows})", got, got_lse, ref, ref_lse)
