@@ -1,0 +1,617 @@
+// attn_tc.cuh -- split-KV decode attention on the 5th-generation tensor cores.
+//
+// One CTA handles one (sequence, KV head) pair and one key range (a split);
+// its NR rows (padded to a multiple of 16) are every query that reads this KV
+// head, so each KV byte is read from HBM once per GQA group.  Keys are the
+// MMA's M dimension (128 per tile), which keeps small row counts cheap:
+//
+//   S^T[128 keys x NR]  = K_tile[128 x D] . Q^T            (tcgen05, K-major A and B)
+//   O^T[D x NR]        += V_tile^T[D x 128] . P^T[128 x NR] (tcgen05, MN-major A and B)
+//   L^T[128 x NR]      += ONES[128 x 128] . P^T             (row sums of P, every lane alike)
+//
+// S (double-buffered), O and L live in tensor memory.  Warp roles (10 warps):
+//   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
+//               shared-memory slots, K_t then V_t;
+//   warp 1    : allocates tensor memory; one lane issues whichever MMA is ready
+//               (S for the next tile, or P.V for the oldest tile whose P is
+//               written) and commits it to mbarriers;
+//   warps 2-9 : softmax -- one key per thread (a tensor-memory lane), two warps
+//               per lane quadrant each owning half of the rows: scale and mask
+//               the logits, keep a running row maximum that is raised (with a
+//               rescale of O and L) only when a logit exceeds it by more than
+//               2^8, write P^T to shared memory as two bf16 parts
+//               (hi = bf16(p), lo = bf16(p - hi)), and finally normalise and
+//               store the output.  P^T is double-buffered when shared memory
+//               allows, so the softmax of tile t+1 overlaps P_t.V_t.
+// Masks: verification is causal (query i sees positions <= seq_len - n_q + i);
+// the draft sees a ring slot iff its tag t satisfies 0 <= t <= p and
+// (t < sink or t > p - window).  Keys masked for every row get their V row
+// zeroed in shared memory before the P.V product, so stale cache bytes (even
+// NaN patterns) cannot leak through 0 * NaN.  Padding rows (past the real
+// rows) see all-zero queries and are never stored.  Every wait is bounded.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+#include "wm_internal.h"
+#include "../../include/wm_api.h"
+
+namespace wm {
+
+constexpr int kTcKeyTile = 128;
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
+
+template <int D, int NR, int NPB>
+struct TcLayout {
+    static constexpr int TK = kTcKeyTile;
+    static constexpr int NCH = D / 64;                         // 128-byte column chunks of a row
+    static constexpr int NOC = D / 128;                        // O accumulators (M = 128 each)
+    static constexpr int REGION = TK * 128;                    // one 64-column chunk of a tile
+    static constexpr int SLOT_BYTES = TK * D * 2;              // one K or V tile
+    static constexpr int NSLOT = kStagingBytes / SLOT_BYTES;   // 4 (D=128) or 2 (D=256)
+    static constexpr int Q_OFF = NSLOT * SLOT_BYTES;
+    static constexpr int Q_REGION = NR * 128;
+    static constexpr int PT_OFF = Q_OFF + NCH * Q_REGION;      // NPB x (P^T hi, P^T lo)
+    static constexpr int PT_BYTES = TK * 128;
+    static constexpr int ONES_OFF = PT_OFF + 2 * NPB * PT_BYTES;
+    static constexpr int ONES_BYTES = 4096;                    // 128 x 16 bf16 ones
+    static constexpr int RED_OFF = ONES_OFF + ONES_BYTES;      // float red[4][64]
+    static constexpr int FLAG_OFF = RED_OFF + 4 * 64 * 4;      // int flags[32]
+    static constexpr int BAR_OFF = FLAG_OFF + 128;
+    static constexpr int NBAR = 2 * NSLOT + 10;
+    static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int TOTAL = TPTR_OFF + 16 + 1024;
+};
+
+template <int D, int NR>
+struct TcCfg {
+    // Double-buffer P^T when both buffers fit in shared memory.
+    static constexpr int NPB = TcLayout<D, NR, 2>::TOTAL <= 227 * 1024 ? 2 : 1;
+    using L = TcLayout<D, NR, NPB>;
+    static constexpr int TK = L::TK, NCH = L::NCH, NOC = L::NOC, REGION = L::REGION;
+    static constexpr int SLOT_BYTES = L::SLOT_BYTES, NSLOT = L::NSLOT;
+    static constexpr int Q_OFF = L::Q_OFF, Q_REGION = L::Q_REGION, PT_OFF = L::PT_OFF, PT_BYTES = L::PT_BYTES;
+    static constexpr int ONES_OFF = L::ONES_OFF, ONES_BYTES = L::ONES_BYTES, RED_OFF = L::RED_OFF;
+    static constexpr int FLAG_OFF = L::FLAG_OFF, BAR_OFF = L::BAR_OFF, TPTR_OFF = L::TPTR_OFF, TOTAL = L::TOTAL;
+    static constexpr int HR = NR / 2;                          // rows per softmax half
+    static constexpr int S_COL = 0;                            // 2 x NR
+    static constexpr int O_COL = 2 * NR;                       // NOC x NR
+    static constexpr int L_COL = O_COL + NOC * NR;             // NR
+    static constexpr int TMEM_USED = L_COL + NR;
+    static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+    static_assert(D == 128 || D == 256, "tensor-core path covers head_dim 128 and 256");
+    static_assert(NR % 16 == 0 && NR >= 16 && NR <= 64, "rows per KV head");
+    static_assert(NSLOT >= 2, "need at least a K and a V slot");
+    static_assert(Q_OFF % 1024 == 0 && PT_OFF % 1024 == 0 && ONES_OFF % 1024 == 0, "1024-byte regions");
+    static_assert(TOTAL <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void tc_report(int32_t *err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+template <int D, int NR>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const AttnParams p) {
+    using C = TcCfg<D, NR>;
+    constexpr int TK = C::TK;
+    constexpr int HR = C::HR;
+    constexpr int NPB = C::NPB;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *gb = smem_raw + (sbase - raw);
+    const uint32_t sQ = sbase + C::Q_OFF;
+    const uint32_t sPT = sbase + C::PT_OFF;
+    const uint32_t sOnes = sbase + C::ONES_OFF;
+    float *red = reinterpret_cast<float *>(gb + C::RED_OFF);                   // [4][64]
+    volatile int *flags = reinterpret_cast<volatile int *>(gb + C::FLAG_OFF);  // [0] abort, [8 + 8*buf + w] votes
+    const uint32_t bars = sbase + C::BAR_OFF;
+    const uint32_t bar_full0 = bars;                          // [NSLOT]
+    const uint32_t bar_empty0 = bars + 8 * C::NSLOT;          // [NSLOT]
+    const uint32_t bar_sfull = bars + 16 * C::NSLOT;          // [2]
+    const uint32_t bar_sfree = bar_sfull + 16;                // [2]
+    const uint32_t bar_pfull = bar_sfree + 16;                // [2]
+    const uint32_t bar_odone = bar_pfull + 16;                // [2]
+    const uint32_t bar_qfull = bar_odone + 16;
+    const uint32_t bar_final = bar_qfull + 8;
+    uint32_t *tptr = reinterpret_cast<uint32_t *>(gb + C::TPTR_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.y;
+    const int b = unit / p.n_kv_heads;
+    const int kvh = unit - b * p.n_kv_heads;
+    const int split = blockIdx.x;
+
+    pdl_wait();  // every global access below may depend on the previous kernel
+    pdl_launch_dependents();
+
+    int64_t n_keys, qpos0;
+    if (p.source == KEYS_RING) {
+        int64_t seen = p.n_seen[b];
+        if (seen < 0) {
+            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
+            seen = 0;
+        }
+        n_keys = p.n_slots;
+        qpos0 = seen - 1;
+    } else {
+        int64_t len = p.seq_lens[b];
+        if (len < 0 || len > p.capacity) {
+            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
+            len = len < 0 ? 0 : p.capacity;
+        }
+        n_keys = len;
+        qpos0 = len - p.n_q;
+    }
+    const int64_t k_begin = (int64_t)split * p.keys_per_split;
+    const int64_t k_end = min(k_begin + (int64_t)p.keys_per_split, n_keys);
+    const int n_tiles = k_end > k_begin ? (int)((k_end - k_begin + TK - 1) / TK) : 0;
+
+    if (n_tiles == 0) {
+        // An empty split (past the end of a shorter sequence): record "no keys"
+        // for its rows and leave without touching tensor memory.
+        for (int r = threadIdx.x; r < p.rows; r += kTcThreads) {
+            const int qi = r / p.group, hh = r - qi * p.group;
+            const int64_t orow = ((int64_t)b * p.n_q + qi) * p.n_q_heads + kvh * p.group + hh;
+            if (p.o_part) {
+                p.lse_part[orow * p.n_split + split] = -CUDART_INF_F;
+            } else {
+                if (p.lse) p.lse[orow] = -CUDART_INF_F;
+                for (int d = 0; d < D; ++d) static_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(0.f);
+            }
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar_full0 + 8 * s, 1);
+            mbar_init(bar_empty0 + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_sfull + 8 * i, 1);
+            mbar_init(bar_sfree + 8 * i, kTcSoftmaxWarps);
+            mbar_init(bar_pfull + 8 * i, kTcSoftmaxWarps);
+            mbar_init(bar_odone + 8 * i, 1);
+        }
+        mbar_init(bar_qfull, kTcSoftmaxWarps);
+        mbar_init(bar_final, 1);
+        for (int i = 0; i < 32; ++i) flags[i] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tptr), C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < C::ONES_BYTES / 16; i += kTcThreads)  // bf16 1.0 = 0x3f80
+        st_shared_v4(sOnes + 16 * i, make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u));
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tptr;
+
+    if (warp == 0) {
+        // ======================================================== TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+            const uint64_t policy = l2_policy_evict_first();
+            int issued = 0;
+            int32_t last_page = 0;
+            for (int u = 0; u < 2 * n_tiles; ++u) {
+                const int s = u % C::NSLOT;
+                if (u >= C::NSLOT &&
+                    !mbar_wait_bounded(bar_empty0 + 8 * s, ((u / C::NSLOT) & 1) ^ 1, kWaitLimit)) {
+                    tc_report(p.err, WM_DEVERR_TIMEOUT);
+                    flags[0] = 1;
+                    break;
+                }
+                if (flags[0]) break;
+                const int t = u >> 1;
+                const CUtensorMap *map = (u & 1) ? &tmv : &tmk;
+                const uint32_t dst = sbase + s * C::SLOT_BYTES;
+                const int64_t key0 = k_begin + (int64_t)t * TK;
+                mbar_arrive_expect_tx(bar_full0 + 8 * s, C::SLOT_BYTES);
+                for (int h = 0; h < TK / p.box_rows; ++h) {
+                    const int64_t kh = key0 + (int64_t)h * p.box_rows;
+                    int c_row, c_outer;
+                    if (p.source == KEYS_PAGED) {
+                        if (kh < n_keys) {
+                            int32_t page = p.block_table[(int64_t)b * p.max_pages + kh / p.page_size];
+                            if (page < 0 || page >= p.n_pages) {
+                                tc_report(p.err, WM_DEVERR_BAD_PAGE);
+                                page = 0;
+                            }
+                            last_page = page;
+                        }
+                        c_row = (int)(kh % p.page_size);  // past the end: any valid page, masked later
+                        c_outer = last_page;
+                    } else {
+                        c_row = (int)kh;
+                        c_outer = b;
+                    }
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d(dst + c * C::REGION + h * p.box_rows * 128, map, bar_full0 + 8 * s, c * 64,
+                                    c_row, kvh, c_outer, policy);
+                }
+                issued = u + 1;
+            }
+            for (int u = max(0, issued - C::NSLOT); u < issued; ++u)
+                mbar_wait_bounded(bar_full0 + 8 * (u % C::NSLOT), (u / C::NSLOT) & 1, kWaitLimit);
+        }
+    } else if (warp == 1) {
+        // ======================================================== MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t id_s = tc::idesc_bf16(128, NR, 0, 0);
+            constexpr uint32_t id_pv = tc::idesc_bf16(128, NR, 1, 1);
+            constexpr uint32_t id_l = tc::idesc_bf16(128, NR, 0, 1);
+            bool ok = mbar_wait_bounded(bar_qfull, 0, kWaitLimit);
+            // Issue whichever product is ready -- S for the next tile (its K
+            // landed and its tensor-memory buffer is free) or P.V for the
+            // oldest tile whose P is written -- so that neither waits on the
+            // other's inputs.
+            int ts = 0, tp = 0;
+            uint32_t idle = 0;
+            const uint64_t ones = tc::smem_desc(sOnes, 128, 256, tc::SWIZZLE_NONE);
+            while (ok && tp < n_tiles) {
+                if (flags[0]) break;
+                bool did = false;
+                if (ts < n_tiles) {
+                    const int uk = 2 * ts, sk = uk % C::NSLOT;
+                    if (mbar_test(bar_full0 + 8 * sk, (uk / C::NSLOT) & 1) &&
+                        (ts < 2 || mbar_test(bar_sfree + 8 * (ts & 1), ((ts - 2) >> 1) & 1))) {
+                        tc::fence_after_sync();
+                        const uint32_t d_s = tmem + C::S_COL + (ts & 1) * NR;
+                        const uint32_t a_k = sbase + sk * C::SLOT_BYTES;
+#pragma unroll
+                        for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t a =
+                                    tc::smem_desc(a_k + c * C::REGION + kk * 32, 16, 1024, tc::SWIZZLE_128B);
+                                const uint64_t bq =
+                                    tc::smem_desc(sQ + c * C::Q_REGION + kk * 32, 16, 1024, tc::SWIZZLE_128B);
+                                tc::mma_f16_ss(d_s, a, bq, id_s, (c | kk) != 0);
+                            }
+                        tc::commit(bar_sfull + 8 * (ts & 1));
+                        tc::commit(bar_empty0 + 8 * sk);
+                        ++ts;
+                        did = true;
+                    }
+                }
+                if (tp < ts) {
+                    const int uv = 2 * tp + 1, sv = uv % C::NSLOT;
+                    if (mbar_test(bar_pfull + 8 * (tp & 1), (tp >> 1) & 1) &&
+                        mbar_test(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1)) {
+                        tc::fence_after_sync();
+                        const uint32_t a_v = sbase + sv * C::SLOT_BYTES;
+                        const uint32_t pt = sPT + (tp % NPB) * 2 * C::PT_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < TK / 16; ++kk) {
+                            const uint32_t first = (tp == 0 && kk == 0) ? 0u : 1u;
+                            const uint64_t b_hi = tc::smem_desc(pt + kk * 2048, C::PT_BYTES, 1024, tc::SWIZZLE_128B);
+                            const uint64_t b_lo =
+                                tc::smem_desc(pt + C::PT_BYTES + kk * 2048, C::PT_BYTES, 1024, tc::SWIZZLE_128B);
+#pragma unroll
+                            for (int m = 0; m < C::NOC; ++m) {
+                                const uint64_t a = tc::smem_desc(a_v + 2 * m * C::REGION + kk * 2048, C::REGION,
+                                                                 1024, tc::SWIZZLE_128B);
+                                const uint32_t d_o = tmem + C::O_COL + m * NR;
+                                tc::mma_f16_ss(d_o, a, b_hi, id_pv, first);
+                                tc::mma_f16_ss(d_o, a, b_lo, id_pv, 1u);
+                            }
+                            tc::mma_f16_ss(tmem + C::L_COL, ones, b_hi, id_l, first);
+                            tc::mma_f16_ss(tmem + C::L_COL, ones, b_lo, id_l, 1u);
+                        }
+                        tc::commit(bar_odone + 8 * (tp & 1));
+                        tc::commit(bar_empty0 + 8 * sv);
+                        ++tp;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle = 0;
+                } else if (++idle > kWaitLimit) {
+                    ok = false;
+                } else if (idle > 64) {
+                    __nanosleep(32);
+                }
+            }
+            if (!ok) {
+                tc_report(p.err, WM_DEVERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            tc::commit(bar_final);  // every MMA issued above has completed once this fires
+            mbar_wait_bounded(bar_final, 0, kWaitLimit);
+        }
+    } else {
+        // ======================================================== softmax warps
+        const int sw = warp - 2;                       // 0..7
+        const int q4 = warp & 3;                       // tensor-memory lane quadrant
+        const int r0 = (sw >> 2) * HR;                 // first row of this warp's half
+        const int kt = 32 * q4 + lane;                 // key within the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const int ct = threadIdx.x - 64;               // 0..255
+        {
+            const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+            constexpr int VPR = D / 8;
+            for (int idx = ct; idx < NR * VPR; idx += 32 * kTcSoftmaxWarps) {
+                const int r = idx / VPR, v = idx - (idx / VPR) * VPR;
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                if (r < p.rows) {
+                    const int i = r / p.group, hh = r - i * p.group;
+                    const int64_t row = ((int64_t)b * p.n_q + i) * p.n_q_heads + kvh * p.group + hh;
+                    val = __ldg(reinterpret_cast<const uint4 *>(q + row * D) + v);
+                }
+                st_shared_v4(sQ + (v >> 3) * C::Q_REGION + swz128(r, v & 7), val);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qfull);
+        }
+        const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
+        // Causal limit of each of this half's rows relative to the query base.
+        int row_off[HR];
+#pragma unroll
+        for (int i = 0; i < HR; ++i) row_off[i] = (r0 + i) / p.group;
+        float m_run[HR];
+#pragma unroll
+        for (int i = 0; i < HR; ++i) m_run[i] = -CUDART_INF_F;
+
+        for (int t = 0; t < n_tiles; ++t) {
+            const int64_t key0 = k_begin + (int64_t)t * TK;
+            const int64_t kabs = key0 + kt;
+            bool key_ok = kabs < k_end;
+            if (key_ok && tags) {
+                const int64_t tg = tags[kabs];
+                key_ok = tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
+            }
+            float s[HR];
+            bool live = !flags[0];
+            if (live && !mbar_wait_bounded(bar_sfull + 8 * (t & 1), (t >> 1) & 1, kWaitLimit)) {
+                tc_report(p.err, WM_DEVERR_TIMEOUT);
+                flags[0] = 1;
+                live = false;
+            }
+            if (live) {
+#pragma unroll
+                for (int c = 0; c < HR / 8; ++c)
+                    tc::ld_32x32b_x8(tmem + lane_off + C::S_COL + (t & 1) * NR + r0 + 8 * c, s + 8 * c);
+                tc::wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < HR; ++i) s[i] = -CUDART_INF_F;
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sfree + 8 * (t & 1));
+
+            // scale to base 2; mask only tiles that reach a boundary
+            const bool causal_tile = p.source != KEYS_RING && key0 + TK - 1 > qpos0;
+            const bool key_tile = tags != nullptr || key0 + TK > k_end;
+            const int64_t rel = qpos0 - kabs;  // key visible to row i iff rel + row_off[i] >= 0
+            bool need = false;
+#pragma unroll
+            for (int i = 0; i < HR; ++i) {
+                bool ok = true;
+                if (key_tile) ok = key_ok;
+                if (causal_tile) ok = ok && rel + row_off[i] >= 0;
+                const float v = ok ? s[i] * p.scale_log2 : -CUDART_INF_F;
+                s[i] = v;
+                need |= v > m_run[i] + kLazyRescale;
+            }
+            const unsigned any = __ballot_sync(0xffffffffu, need);
+            if (lane == 0) flags[8 + 8 * (t & 1) + sw] = any != 0u;
+            named_bar_sync(1, 32 * kTcSoftmaxWarps);
+            int votes = 0;
+#pragma unroll
+            for (int w = 0; w < kTcSoftmaxWarps; ++w) votes |= flags[8 + 8 * (t & 1) + w];
+            const bool rescale = votes != 0;
+            if (rescale) {
+#pragma unroll
+                for (int i = 0; i < HR; ++i) {
+                    float mx = s[i];
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0) red[64 * q4 + r0 + i] = mx;
+                }
+            }
+            named_bar_sync(1, 32 * kTcSoftmaxWarps);
+            bool o_stable = t == 0;  // P_{t-1}.V_{t-1} known complete
+            if (rescale) {
+                float alpha[HR];
+#pragma unroll
+                for (int i = 0; i < HR; ++i) {
+                    const int r = r0 + i;
+                    const float m_new = fmaxf(m_run[i], fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r])));
+                    const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+                    alpha[i] = ex2(m_run[i] - m_use);
+                    m_run[i] = m_new;
+                }
+                if (t > 0) {
+                    // O and L hold tiles 0..t-1 at the old maximum: wait for P_{t-1}.V_{t-1}, then rescale
+                    if (!flags[0] && !mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit)) {
+                        tc_report(p.err, WM_DEVERR_TIMEOUT);
+                        flags[0] = 1;
+                    }
+                    o_stable = true;
+                    tc::fence_after_sync();
+                    if (!flags[0]) {
+#pragma unroll
+                        for (int a = 0; a <= C::NOC; ++a) {
+                            const uint32_t col = (a < C::NOC ? C::O_COL + a * NR : C::L_COL) + r0;
+#pragma unroll
+                            for (int c = 0; c < HR / 8; ++c) {
+                                float v8[8];
+                                tc::ld_32x32b_x8(tmem + lane_off + col + 8 * c, v8);
+                                tc::wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v8[i] *= alpha[8 * c + i];
+                                tc::st_32x32b_x8(tmem + lane_off + col + 8 * c, v8);
+                            }
+                        }
+                        tc::wait_st();
+                    }
+                }
+            }
+
+            // P = 2^(s - m) as bf16 hi + lo parts into P^T[key][row]
+            uint32_t hi_w[HR / 2], lo_w[HR / 2];
+#pragma unroll
+            for (int i = 0; i < HR; i += 2) {
+                const float ma = m_run[i] == -CUDART_INF_F ? 0.f : m_run[i];
+                const float mb = m_run[i + 1] == -CUDART_INF_F ? 0.f : m_run[i + 1];
+                const float pa = ex2(s[i] - ma), pb = ex2(s[i + 1] - mb);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(pa, pb);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __low2float(h), pb - __high2float(h));
+                hi_w[i / 2] = *reinterpret_cast<const uint32_t *>(&h);
+                lo_w[i / 2] = *reinterpret_cast<const uint32_t *>(&l);
+            }
+            // the P^T buffer of this tile was last read by P_{t-NPB}.V_{t-NPB}
+            if (t >= NPB && !(NPB == 1 && o_stable) && !flags[0] &&
+                !mbar_wait_bounded(bar_odone + 8 * ((t - NPB) & 1), ((t - NPB) >> 1) & 1, kWaitLimit)) {
+                tc_report(p.err, WM_DEVERR_TIMEOUT);
+                flags[0] = 1;
+            }
+            const uint32_t pt = sPT + (t % NPB) * 2 * C::PT_BYTES;
+#pragma unroll
+            for (int j = 0; j < HR / 8; ++j) {
+                const int chunk = r0 / 8 + j;
+                const uint32_t off = (uint32_t)kt * 128u + ((uint32_t)(chunk ^ (kt & 7)) << 4);
+                st_shared_v4(pt + off, make_uint4(hi_w[4 * j], hi_w[4 * j + 1], hi_w[4 * j + 2], hi_w[4 * j + 3]));
+                st_shared_v4(pt + C::PT_BYTES + off,
+                             make_uint4(lo_w[4 * j], lo_w[4 * j + 1], lo_w[4 * j + 2], lo_w[4 * j + 3]));
+            }
+            if (!key_ok && r0 == 0 && !flags[0]) {
+                // a key no row may see: zero its V row once the V tile has landed
+                const int uv = 2 * t + 1, sv = uv % C::NSLOT;
+                if (mbar_wait_bounded(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1, kWaitLimit)) {
+                    const uint32_t vrow = sbase + sv * C::SLOT_BYTES;
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(vrow + c * C::REGION + swz128(kt, j), make_uint4(0u, 0u, 0u, 0u));
+                } else {
+                    tc_report(p.err, WM_DEVERR_TIMEOUT);
+                    flags[0] = 1;
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_pfull + 8 * (t & 1));
+        }
+
+        // ---- epilogue: this thread owns tensor-memory lane d = 32*q4 + lane of every O block
+        if (n_tiles > 0 && !flags[0] &&
+            !mbar_wait_bounded(bar_odone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, kWaitLimit)) {
+            tc_report(p.err, WM_DEVERR_TIMEOUT);
+            flags[0] = 1;
+        }
+        tc::fence_after_sync();
+        const bool have = n_tiles > 0 && !flags[0];
+        const float kLn2 = 0.693147180559945309f;
+#pragma unroll
+        for (int c = 0; c < HR / 8; ++c) {
+            float l8[8];
+            if (have) {
+                tc::ld_32x32b_x8(tmem + lane_off + C::L_COL + r0 + 8 * c, l8);
+                tc::wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < C::NOC; ++m) {
+                float o8[8];
+                if (have) {
+                    tc::ld_32x32b_x8(tmem + lane_off + C::O_COL + m * NR + r0 + 8 * c, o8);
+                    tc::wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o8[i] = 0.f;
+                }
+                const int d = m * 128 + 32 * q4 + lane;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + 8 * c + i;
+                    if (r >= p.rows) continue;
+                    const float lt = l8[i];
+                    const float o = lt > 0.f ? o8[i] / lt : 0.f;
+                    const int qi = r / p.group, hh = r - qi * p.group;
+                    const int64_t orow = ((int64_t)b * p.n_q + qi) * p.n_q_heads + kvh * p.group + hh;
+                    if (p.o_part)
+                        p.o_part[(orow * p.n_split + split) * D + d] = o;
+                    else
+                        static_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(o);
+                }
+            }
+            // lse of row r is written by the thread that owns tensor-memory lane r
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + 8 * c + i;
+                if (r >= p.rows || kt != r) continue;
+                const float lt = l8[i];
+                const float lse = lt > 0.f ? (m_run[8 * c + i] + lg2(lt)) * kLn2 : -CUDART_INF_F;
+                const int qi = r / p.group, hh = r - qi * p.group;
+                const int64_t orow = ((int64_t)b * p.n_q + qi) * p.n_q_heads + kvh * p.group + hh;
+                if (p.o_part)
+                    p.lse_part[orow * p.n_split + split] = lse;
+                else if (p.lse)
+                    p.lse[orow] = lse;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, int NR>
+cudaError_t launch_attn_tc_nr(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                              cudaStream_t stream) {
+    constexpr int smem = TcCfg<D, NR>::TOTAL;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
+    return launch_pdl(attn_tc_kernel<D, NR>, grid, dim3(kTcThreads), smem, stream, k, v, p);
+}
+
+template <int D>
+cudaError_t launch_attn_tc(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int n_rows16,
+                           cudaStream_t stream) {
+    switch (n_rows16) {
+        case 16: return launch_attn_tc_nr<D, 16>(k, v, p, stream);
+        case 32: return launch_attn_tc_nr<D, 32>(k, v, p, stream);
+        case 48: return launch_attn_tc_nr<D, 48>(k, v, p, stream);
+        case 64: return launch_attn_tc_nr<D, 64>(k, v, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace wm

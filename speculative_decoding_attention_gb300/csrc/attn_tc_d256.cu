@@ -1,0 +1,11 @@
+// attn_tc_d256.cu -- tensor-core attention kernel instantiations for head_dim 256.
+#include "attn_tc.cuh"
+
+namespace wm {
+
+cudaError_t launch_attn_tc_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int n_rows16,
+                               cudaStream_t stream) {
+    return launch_attn_tc<256>(k, v, p, n_rows16, stream);
+}
+
+}  // namespace wm

@@ -2,7 +2,7 @@
 //
 // Per row r with parts s = 0..n-1 (each part normalised by its own softmax sum):
 //   M = max_s lse_s,  lse = M + ln sum_s exp(lse_s - M),  o = sum_s exp(lse_s - lse) o_s.
-// A part with lse = -inf holds no key and gets weight 0.
+// A part with lse = -inf holds no key; it gets weight 0 and its o is not read.
 //
 // One CTA per (row, 32-column block).  Its 128 threads are 8 column threads
 // (one float4 each) x 16 part groups, so the loads of different parts are
@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll 4
         for (int s = pg; s < n_parts; s += kPartGroups) {
             const float w = ex2((ls[s] - lse) * kLog2e);
+            if (w == 0.f) continue;  // empty part (lse -inf): its o is never read
             const float4 v = __ldg(reinterpret_cast<const float4 *>(op + (int64_t)s * head_dim));
             acc.x += w * v.x;
             acc.y += w * v.y;

@@ -59,15 +59,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A 4-d view [outer][heads][inner][D] of bf16 rows, read in boxes of
-// 64 columns x kKeyTile rows with the 128-byte swizzle.
-bool encode_kv_map(CUtensorMap *map, const void *base, int head_dim, int64_t inner, int heads,
-                   int64_t outer) {
+// 64 columns x box_rows rows with the 128-byte swizzle.
+bool encode_kv_map(CUtensorMap *map, const void *base, int head_dim, int64_t inner, int heads, int64_t outer,
+                   int box_rows) {
     auto encode = tensor_map_encoder();
     if (!encode) return false;
     const cuuint64_t row = (cuuint64_t)head_dim * 2;
     cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)inner, (cuuint64_t)heads, (cuuint64_t)outer};
     cuuint64_t strides[3] = {row, row * (cuuint64_t)inner, row * (cuuint64_t)inner * (cuuint64_t)heads};
-    cuuint32_t box[4] = {64, (cuuint32_t)kKeyTile, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t elem[4] = {1, 1, 1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
                               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -84,20 +84,35 @@ struct SplitPlan {
     int keys_per_split = 0;
 };
 
-// Key splits for `units` (sequence, KV head) pairs over up to max_keys keys:
-// by default one wave of one CTA per SM, never a split smaller than a tile.
-SplitPlan plan_splits(int units, int64_t max_keys, int requested) {
+// Keys per tile of the attention kernel that serves this head dim: the
+// tensor-core kernel (128) for 128 and 256, the mma.sync kernel (64) for 64.
+int key_tile(int head_dim) { return head_dim == 64 ? kKeyTile : kTcTile; }
+
+// K+V bytes per split when a batch may be ragged (see plan_splits).
+constexpr int64_t kRaggedSplitBytes = 8ll << 20;
+
+// Key splits for `units` (sequence, KV head) pairs over up to max_keys keys,
+// never a split smaller than a tile.  By default: one wave of one CTA per SM.
+// With several sequences the lengths may differ (only their maximum is known
+// on the host), so splits are also capped at about kRaggedSplitBytes of K+V:
+// short sequences then leave most of their splits empty (those CTAs exit at
+// once) and the block scheduler balances the rest.
+SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim) {
     SplitPlan pl;
-    const int64_t tiles = std::max<int64_t>(1, (max_keys + kKeyTile - 1) / kKeyTile);
+    const int64_t tiles = std::max<int64_t>(1, (max_keys + tile - 1) / tile);
     int64_t ns = requested;
     if (ns <= 0) {
         const int sms = sm_count();
         ns = std::max<int64_t>(1, (sms > 0 ? sms : 1) / std::max(1, units));
+        if (batch > 1) {
+            const int64_t keys_cap = std::max<int64_t>(tile, kRaggedSplitBytes / (4 * head_dim) / tile * tile);
+            ns = std::max<int64_t>(ns, (max_keys + keys_cap - 1) / keys_cap);
+        }
     }
     ns = std::min<int64_t>(ns, tiles);
     const int64_t tps = (tiles + ns - 1) / ns;
     pl.n_split = (int)((tiles + tps - 1) / tps);
-    pl.keys_per_split = (int)(tps * kKeyTile);
+    pl.keys_per_split = (int)(tps * tile);
     return pl;
 }
 
@@ -107,12 +122,12 @@ size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
     return o_aligned + (size_t)rows_total * n_split * sizeof(float);
 }
 
-cudaError_t launch_attn_any(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                            cudaStream_t st) {
+cudaError_t launch_attn_any(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, cudaStream_t st) {
+    const int m_tiles = (p.rows + 15) / 16;
     switch (p.head_dim) {
         case 64: return launch_attn_d64(k, v, p, m_tiles, st);
-        case 128: return launch_attn_d128(k, v, p, m_tiles, st);
-        case 256: return launch_attn_d256(k, v, p, m_tiles, st);
+        case 128: return launch_attn_tc_d128(k, v, p, 16 * m_tiles, st);
+        case 256: return launch_attn_tc_d256(k, v, p, 16 * m_tiles, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -134,7 +149,7 @@ wm_status kv_check(const wm_kv *kv, bool need_tile_pages) {
     if (kv->block_table) {
         if (kv->page_size <= 0 || kv->max_pages <= 0 || kv->n_pages <= 0 || !aligned(kv->block_table, 4))
             return WM_ERR_INVALID_ARG;
-        if (need_tile_pages && kv->page_size % kKeyTile) return WM_ERR_UNSUPPORTED;
+        if (need_tile_pages && kv->page_size % kKeyTile) return WM_ERR_UNSUPPORTED;  // whole 64-key boxes
         if (kv->n_pages > INT32_MAX) return WM_ERR_UNSUPPORTED;
     } else if (kv->n_cap <= 0 || kv->n_cap > INT32_MAX) {
         return kv->n_cap <= 0 ? WM_ERR_INVALID_ARG : WM_ERR_UNSUPPORTED;
@@ -170,7 +185,7 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
     if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY) || batch <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 ||
         n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
         return 0;
-    return plan_splits(batch * n_kv_heads, max_keys, n_split).n_split;
+    return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(head_dim), head_dim).n_split;
 }
 
 size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
@@ -252,7 +267,8 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
 static wm_status run_attention(AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv, int64_t max_keys,
                                int32_t n_split, void *out, float *lse, void *ws, size_t ws_bytes,
                                cudaStream_t st) {
-    const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, max_keys, n_split);
+    const SplitPlan pl =
+        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(p.head_dim), p.head_dim);
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
     p.n_split = pl.n_split;
     p.keys_per_split = pl.keys_per_split;
@@ -267,8 +283,7 @@ static wm_status run_attention(AttnParams &p, const CUtensorMap &mk, const CUten
         p.o_part = static_cast<float *>(ws);
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + ((o + 255) & ~(size_t)255));
     }
-    const int m_tiles = (p.rows + 15) / 16;
-    cudaError_t e = launch_attn_any(mk, mv, p, m_tiles, st);
+    cudaError_t e = launch_attn_any(mk, mv, p, st);
     if (e != cudaSuccess) return WM_ERR_CUDA;
     if (pl.n_split > 1) {
         e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, st);
@@ -288,9 +303,10 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
     int32_t *err = device_error_ptr();
     if (!err) return WM_ERR_CUDA;
     const int n_slots = ring->sink + ring->window;
+    const int box = key_tile(ring->head_dim);
     CUtensorMap mk, mv;
-    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch) ||
-        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch))
+    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box) ||
+        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box))
         return WM_ERR_CUDA;
     AttnParams p;
     std::memset(&p, 0, sizeof p);
@@ -304,6 +320,7 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
     p.sink = ring->sink;
     p.window = ring->window;
     p.capacity = n_slots;
+    p.box_rows = box;
     p.q = q;
     p.n_q = 1;
     p.n_q_heads = n_q_heads;
@@ -333,8 +350,10 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     CUtensorMap mk, mv;
     const int64_t inner = paged ? kv->page_size : kv->n_cap;
     const int64_t outer = paged ? kv->n_pages : kv->batch;
-    if (!encode_kv_map(&mk, kv->k, kv->head_dim, inner, kv->n_kv_heads, outer) ||
-        !encode_kv_map(&mv, kv->v, kv->head_dim, inner, kv->n_kv_heads, outer))
+    const int tile = key_tile(kv->head_dim);
+    const int box = paged && kv->page_size % tile ? kKeyTile : tile;  // a box never crosses a page
+    if (!encode_kv_map(&mk, kv->k, kv->head_dim, inner, kv->n_kv_heads, outer, box) ||
+        !encode_kv_map(&mv, kv->v, kv->head_dim, inner, kv->n_kv_heads, outer, box))
         return WM_ERR_CUDA;
     AttnParams p;
     std::memset(&p, 0, sizeof p);
@@ -348,6 +367,7 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     p.n_pages = kv->n_pages;
     p.page_size = kv->page_size;
     p.max_pages = kv->max_pages;
+    p.box_rows = box;
     p.q = q;
     p.n_q = n_q;
     p.n_q_heads = n_q_heads;

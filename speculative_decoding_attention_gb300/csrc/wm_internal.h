@@ -36,6 +36,7 @@ struct AttnParams {
     int64_t n_pages;
     int32_t page_size;
     int32_t max_pages;
+    int32_t box_rows;     // key rows per TMA box (64, or 128 for the tensor-core kernel)
     // draft (ring)
     const int32_t *pos_tag;
     const int64_t *n_seen;
@@ -51,7 +52,7 @@ struct AttnParams {
     float scale_log2;     // scale * log2(e)
     // split
     int32_t n_split;
-    int32_t keys_per_split;  // multiple of kKeyTile
+    int32_t keys_per_split;  // multiple of the kernel's key tile
     // outputs
     void *out;            // bf16, same layout as q
     float *lse;           // [B][n_q][Hq] or NULL
@@ -67,6 +68,14 @@ cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const A
                              int m_tiles, cudaStream_t stream);
 cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
                              int m_tiles, cudaStream_t stream);
+
+// Tensor-core (tcgen05) attention kernel for head dims 128 and 256 (attn_tc_d<D>.cu);
+// n_rows16 is the row count per KV head rounded up to 16, 128-key tiles.
+cudaError_t launch_attn_tc_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                                int n_rows16, cudaStream_t stream);
+cudaError_t launch_attn_tc_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                                int n_rows16, cudaStream_t stream);
+constexpr int kTcTile = 128;
 
 // Ring and merge kernels (ring.cu, merge.cu).
 cudaError_t launch_ring_append(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
