@@ -64,6 +64,7 @@ typedef enum wm_status {
 #define WM_DEVERR_BAD_LENGTH 1   /* negative length/position or one beyond capacity */
 #define WM_DEVERR_BAD_PAGE 2     /* block-table entry outside [0, n_pages) */
 #define WM_DEVERR_TIMEOUT 3      /* a pipeline wait exceeded its iteration limit */
+#define WM_DEVERR_INTERNAL 4     /* a kernel's own address-range self-check failed (the access was skipped) */
 
 /*
  * The draft's compact ring buffer (one per draft attention layer).

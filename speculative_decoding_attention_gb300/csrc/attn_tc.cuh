@@ -7,9 +7,12 @@
 //
 //   S^T[128 keys x NR]  = K_tile[128 x D] . Q^T            (tcgen05, K-major A and B)
 //   O^T[D x NR]        += V_tile^T[D x 128] . P^T[128 x NR] (tcgen05, MN-major A and B)
-//   L^T[128 x NR]      += ONES[128 x 128] . P^T             (row sums of P, every lane alike)
 //
-// S (double-buffered), O and L live in tensor memory.  Warp roles (10 warps):
+// S (double-buffered) and O live in tensor memory; the softmax row sums are
+// kept per key-thread in registers and reduced once at the end.  The shared
+// memory split between K/V staging slots and P^T buffers is chosen per head
+// dim and row count: as many staging slots as fit, then a second P^T buffer
+// if it still fits.  Warp roles (10 warps):
 //   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
 //               shared-memory slots, K_t then V_t;
 //   warp 1    : allocates tensor memory; one lane issues whichever MMA is ready
@@ -47,53 +50,74 @@ constexpr int kTcSoftmaxWarps = 8;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
 constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
 
-template <int D, int NR, int NPB>
+template <int D, int NR, int NSLOT_, int NPB_>
 struct TcLayout {
     static constexpr int TK = kTcKeyTile;
+    static constexpr int NSLOT = NSLOT_, NPB = NPB_;
     static constexpr int NCH = D / 64;                         // 128-byte column chunks of a row
     static constexpr int NOC = D / 128;                        // O accumulators (M = 128 each)
     static constexpr int REGION = TK * 128;                    // one 64-column chunk of a tile
     static constexpr int SLOT_BYTES = TK * D * 2;              // one K or V tile
-    static constexpr int NSLOT = kStagingBytes / SLOT_BYTES;   // 4 (D=128) or 2 (D=256)
+    static constexpr int PT_ROW = NR <= 32 ? 64 : 128;         // bytes per key row of P^T
+    static constexpr int PT_SWIZZLE = NR <= 32 ? 4 : 2;        // 64B / 128B swizzle (descriptor code)
+    static constexpr int PT_ATOM = PT_ROW * 8;                 // one 8-key swizzle atom
     static constexpr int Q_OFF = NSLOT * SLOT_BYTES;
     static constexpr int Q_REGION = NR * 128;
     static constexpr int PT_OFF = Q_OFF + NCH * Q_REGION;      // NPB x (P^T hi, P^T lo)
-    static constexpr int PT_BYTES = TK * 128;
-    static constexpr int ONES_OFF = PT_OFF + 2 * NPB * PT_BYTES;
-    static constexpr int ONES_BYTES = 4096;                    // 128 x 16 bf16 ones
-    static constexpr int RED_OFF = ONES_OFF + ONES_BYTES;      // float red[4][64]
-    static constexpr int FLAG_OFF = RED_OFF + 4 * 64 * 4;      // int flags[32]
+    static constexpr int PT_BYTES = TK * PT_ROW;
+    static constexpr int RED_OFF = PT_OFF + 2 * NPB * PT_BYTES;  // float red[4][NR]
+    static constexpr int FLAG_OFF = RED_OFF + 4 * NR * 4;        // int flags[32]
     static constexpr int BAR_OFF = FLAG_OFF + 128;
     static constexpr int NBAR = 2 * NSLOT + 10;
     static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = TPTR_OFF + 16 + 1024;
+    static constexpr bool FITS = TOTAL <= 227 * 1024;
+};
+
+// Shared-memory plan: the most K/V staging slots (up to 4) that fit with one
+// P^T buffer -- keeping HBM requests in flight matters most, and 3 slots
+// already let the next tile's K and V load while this tile computes -- then a
+// second P^T buffer if it fits too.
+template <int D, int NR>
+struct TcPlan {
+    static constexpr int NSLOT = TcLayout<D, NR, 4, 1>::FITS ? 4 : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
+    static constexpr int NPB = TcLayout<D, NR, NSLOT, 2>::FITS ? 2 : 1;
 };
 
 template <int D, int NR>
 struct TcCfg {
-    // Double-buffer P^T when both buffers fit in shared memory.
-    static constexpr int NPB = TcLayout<D, NR, 2>::TOTAL <= 227 * 1024 ? 2 : 1;
-    using L = TcLayout<D, NR, NPB>;
+    using L = TcLayout<D, NR, TcPlan<D, NR>::NSLOT, TcPlan<D, NR>::NPB>;
+    static constexpr int NSLOT = L::NSLOT, NPB = L::NPB;
     static constexpr int TK = L::TK, NCH = L::NCH, NOC = L::NOC, REGION = L::REGION;
-    static constexpr int SLOT_BYTES = L::SLOT_BYTES, NSLOT = L::NSLOT;
+    static constexpr int SLOT_BYTES = L::SLOT_BYTES;
+    static constexpr int PT_ROW = L::PT_ROW, PT_SWIZZLE = L::PT_SWIZZLE, PT_ATOM = L::PT_ATOM;
     static constexpr int Q_OFF = L::Q_OFF, Q_REGION = L::Q_REGION, PT_OFF = L::PT_OFF, PT_BYTES = L::PT_BYTES;
-    static constexpr int ONES_OFF = L::ONES_OFF, ONES_BYTES = L::ONES_BYTES, RED_OFF = L::RED_OFF;
+    static constexpr int RED_OFF = L::RED_OFF;
     static constexpr int FLAG_OFF = L::FLAG_OFF, BAR_OFF = L::BAR_OFF, TPTR_OFF = L::TPTR_OFF, TOTAL = L::TOTAL;
     static constexpr int HR = NR / 2;                          // rows per softmax half
     static constexpr int S_COL = 0;                            // 2 x NR
     static constexpr int O_COL = 2 * NR;                       // NOC x NR
-    static constexpr int L_COL = O_COL + NOC * NR;             // NR
-    static constexpr int TMEM_USED = L_COL + NR;
+    static constexpr int TMEM_USED = O_COL + NOC * NR;
     static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static_assert(D == 128 || D == 256, "tensor-core path covers head_dim 128 and 256");
     static_assert(NR % 16 == 0 && NR >= 16 && NR <= 64, "rows per KV head");
-    static_assert(NSLOT >= 2, "need at least a K and a V slot");
-    static_assert(Q_OFF % 1024 == 0 && PT_OFF % 1024 == 0 && ONES_OFF % 1024 == 0, "1024-byte regions");
-    static_assert(TOTAL <= 227 * 1024, "shared memory budget");
+    static_assert(Q_OFF % 1024 == 0 && PT_OFF % 1024 == 0 && PT_BYTES % 1024 == 0, "1024-byte regions");
+    static_assert(L::FITS, "shared memory budget");
 };
 
 __device__ __forceinline__ void tc_report(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
+}
+
+// The abort flag as lane 0 of the calling warp sees it, so that every lane
+// takes the same branch around warp-collective tcgen05 loads and stores.
+__device__ __forceinline__ bool warp_aborted(volatile int *flags) {
+    return __shfl_sync(0xffffffffu, flags[0], 0) != 0;
+}
+
+// Self-check of a shared-memory range [lo, lo + len) against [base, end).
+__device__ __forceinline__ bool in_smem(uint32_t lo, uint32_t len, uint32_t base, uint32_t end) {
+    return lo >= base && lo + len <= end;
 }
 
 template <int D, int NR>
@@ -111,8 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *gb = smem_raw + (sbase - raw);
     const uint32_t sQ = sbase + C::Q_OFF;
     const uint32_t sPT = sbase + C::PT_OFF;
-    const uint32_t sOnes = sbase + C::ONES_OFF;
-    float *red = reinterpret_cast<float *>(gb + C::RED_OFF);                   // [4][64]
+    float *red = reinterpret_cast<float *>(gb + C::RED_OFF);                   // [4][NR]
     volatile int *flags = reinterpret_cast<volatile int *>(gb + C::FLAG_OFF);  // [0] abort, [8 + 8*buf + w] votes
     const uint32_t bars = sbase + C::BAR_OFF;
     const uint32_t bar_full0 = bars;                          // [NSLOT]
@@ -193,9 +216,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::tmem_alloc(smem_u32(tptr), C::TMEM_COLS);
         tc::tmem_relinquish();
     }
-    for (int i = threadIdx.x; i < C::ONES_BYTES / 16; i += kTcThreads)  // bf16 1.0 = 0x3f80
-        st_shared_v4(sOnes + 16 * i, make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u));
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -241,6 +261,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         c_row = (int)kh;
                         c_outer = b;
                     }
+                    if (!in_smem(dst + (C::NCH - 1) * C::REGION + h * p.box_rows * 128, p.box_rows * 128,
+                                 sbase, sbase + C::NSLOT * C::SLOT_BYTES) ||
+                        c_row < 0 || c_outer < 0) {
+                        tc_report(p.err, WM_DEVERR_INTERNAL);
+                        flags[0] = 1;
+                        break;
+                    }
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d(dst + c * C::REGION + h * p.box_rows * 128, map, bar_full0 + 8 * s, c * 64,
@@ -256,7 +283,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t id_s = tc::idesc_bf16(128, NR, 0, 0);
             constexpr uint32_t id_pv = tc::idesc_bf16(128, NR, 1, 1);
-            constexpr uint32_t id_l = tc::idesc_bf16(128, NR, 0, 1);
             bool ok = mbar_wait_bounded(bar_qfull, 0, kWaitLimit);
             // Issue whichever product is ready -- S for the next tile (its K
             // landed and its tensor-memory buffer is free) or P.V for the
@@ -264,17 +290,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // other's inputs.
             int ts = 0, tp = 0;
             uint32_t idle = 0;
-            const uint64_t ones = tc::smem_desc(sOnes, 128, 256, tc::SWIZZLE_NONE);
             while (ok && tp < n_tiles) {
                 if (flags[0]) break;
                 bool did = false;
                 if (ts < n_tiles) {
                     const int uk = 2 * ts, sk = uk % C::NSLOT;
-                    if (mbar_test(bar_full0 + 8 * sk, (uk / C::NSLOT) & 1) &&
+                    // A parity test cannot tell "this fill landed" from "the fill
+                    // before it has not landed yet" (the parities match), so only
+                    // test once the slot's previous unit is known to have landed:
+                    // its consumer (S for a K unit, P.V for a V unit) was issued.
+                    const int prev = uk - C::NSLOT;
+                    const bool prev_in = prev < 0 || ((prev & 1) ? (prev >> 1) < tp : (prev >> 1) < ts);
+                    if (prev_in && mbar_test(bar_full0 + 8 * sk, (uk / C::NSLOT) & 1) &&
                         (ts < 2 || mbar_test(bar_sfree + 8 * (ts & 1), ((ts - 2) >> 1) & 1))) {
                         tc::fence_after_sync();
                         const uint32_t d_s = tmem + C::S_COL + (ts & 1) * NR;
                         const uint32_t a_k = sbase + sk * C::SLOT_BYTES;
+                        if (!in_smem(a_k, C::SLOT_BYTES, sbase, sbase + C::NSLOT * C::SLOT_BYTES) ||
+                            !in_smem(sQ, C::NCH * C::Q_REGION, sbase + C::Q_OFF, sbase + C::PT_OFF)) {
+                            tc_report(p.err, WM_DEVERR_INTERNAL);
+                            ok = false;
+                            break;
+                        }
 #pragma unroll
                         for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
@@ -293,17 +330,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (tp < ts) {
                     const int uv = 2 * tp + 1, sv = uv % C::NSLOT;
-                    if (mbar_test(bar_pfull + 8 * (tp & 1), (tp >> 1) & 1) &&
+                    const int prev = uv - C::NSLOT;  // see the K test above
+                    const bool prev_in = prev < 0 || ((prev & 1) ? (prev >> 1) < tp : (prev >> 1) < ts);
+                    if (prev_in && mbar_test(bar_pfull + 8 * (tp & 1), (tp >> 1) & 1) &&
                         mbar_test(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1)) {
                         tc::fence_after_sync();
                         const uint32_t a_v = sbase + sv * C::SLOT_BYTES;
                         const uint32_t pt = sPT + (tp % NPB) * 2 * C::PT_BYTES;
+                        if (!in_smem(a_v, C::SLOT_BYTES, sbase, sbase + C::NSLOT * C::SLOT_BYTES) ||
+                            !in_smem(pt, 2 * C::PT_BYTES, sPT, sPT + 2 * NPB * C::PT_BYTES)) {
+                            tc_report(p.err, WM_DEVERR_INTERNAL);
+                            ok = false;
+                            break;
+                        }
 #pragma unroll
                         for (int kk = 0; kk < TK / 16; ++kk) {
                             const uint32_t first = (tp == 0 && kk == 0) ? 0u : 1u;
-                            const uint64_t b_hi = tc::smem_desc(pt + kk * 2048, C::PT_BYTES, 1024, tc::SWIZZLE_128B);
+                            const uint32_t koff = kk * 2 * C::PT_ATOM;  // 16 keys = two 8-key atoms
+                            const uint64_t b_hi =
+                                tc::smem_desc(pt + koff, C::PT_BYTES, C::PT_ATOM, C::PT_SWIZZLE);
                             const uint64_t b_lo =
-                                tc::smem_desc(pt + C::PT_BYTES + kk * 2048, C::PT_BYTES, 1024, tc::SWIZZLE_128B);
+                                tc::smem_desc(pt + C::PT_BYTES + koff, C::PT_BYTES, C::PT_ATOM, C::PT_SWIZZLE);
 #pragma unroll
                             for (int m = 0; m < C::NOC; ++m) {
                                 const uint64_t a = tc::smem_desc(a_v + 2 * m * C::REGION + kk * 2048, C::REGION,
@@ -312,8 +359,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 tc::mma_f16_ss(d_o, a, b_hi, id_pv, first);
                                 tc::mma_f16_ss(d_o, a, b_lo, id_pv, 1u);
                             }
-                            tc::mma_f16_ss(tmem + C::L_COL, ones, b_hi, id_l, first);
-                            tc::mma_f16_ss(tmem + C::L_COL, ones, b_lo, id_l, 1u);
                         }
                         tc::commit(bar_odone + 8 * (tp & 1));
                         tc::commit(bar_empty0 + 8 * sv);
@@ -362,13 +407,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(bar_qfull);
         }
         const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
-        // Causal limit of each of this half's rows relative to the query base.
-        int row_off[HR];
+        float m_run[HR], l_run[HR];  // running max (same in every thread) and this key-thread's sum
 #pragma unroll
-        for (int i = 0; i < HR; ++i) row_off[i] = (r0 + i) / p.group;
-        float m_run[HR];
-#pragma unroll
-        for (int i = 0; i < HR; ++i) m_run[i] = -CUDART_INF_F;
+        for (int i = 0; i < HR; ++i) {
+            m_run[i] = -CUDART_INF_F;
+            l_run[i] = 0.f;
+        }
 
         for (int t = 0; t < n_tiles; ++t) {
             const int64_t key0 = k_begin + (int64_t)t * TK;
@@ -379,12 +423,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 key_ok = tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
             }
             float s[HR];
-            bool live = !flags[0];
+            bool live = !warp_aborted(flags);
             if (live && !mbar_wait_bounded(bar_sfull + 8 * (t & 1), (t >> 1) & 1, kWaitLimit)) {
                 tc_report(p.err, WM_DEVERR_TIMEOUT);
                 flags[0] = 1;
-                live = false;
             }
+            live = !warp_aborted(flags);
+            tc::fence_after_sync();  // order the S loads after the MMA completion observed above
             if (live) {
 #pragma unroll
                 for (int c = 0; c < HR / 8; ++c)
@@ -401,13 +446,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // scale to base 2; mask only tiles that reach a boundary
             const bool causal_tile = p.source != KEYS_RING && key0 + TK - 1 > qpos0;
             const bool key_tile = tags != nullptr || key0 + TK > k_end;
-            const int64_t rel = qpos0 - kabs;  // key visible to row i iff rel + row_off[i] >= 0
+            const int64_t rel = qpos0 - kabs;  // key visible to row r iff rel + r / group >= 0
             bool need = false;
 #pragma unroll
             for (int i = 0; i < HR; ++i) {
                 bool ok = true;
                 if (key_tile) ok = key_ok;
-                if (causal_tile) ok = ok && rel + row_off[i] >= 0;
+                if (causal_tile) ok = ok && rel + (r0 + i) / p.group >= 0;
                 const float v = ok ? s[i] * p.scale_log2 : -CUDART_INF_F;
                 s[i] = v;
                 need |= v > m_run[i] + kLazyRescale;
@@ -425,7 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float mx = s[i];
 #pragma unroll
                     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    if (lane == 0) red[64 * q4 + r0 + i] = mx;
+                    if (lane == 0) red[NR * q4 + r0 + i] = mx;
                 }
             }
             named_bar_sync(1, 32 * kTcSoftmaxWarps);
@@ -435,23 +480,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int i = 0; i < HR; ++i) {
                     const int r = r0 + i;
-                    const float m_new = fmaxf(m_run[i], fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r])));
+                    const float m_new =
+                        fmaxf(m_run[i], fmaxf(fmaxf(red[r], red[NR + r]), fmaxf(red[2 * NR + r], red[3 * NR + r])));
                     const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
                     alpha[i] = ex2(m_run[i] - m_use);
                     m_run[i] = m_new;
+                    l_run[i] *= alpha[i];
                 }
                 if (t > 0) {
-                    // O and L hold tiles 0..t-1 at the old maximum: wait for P_{t-1}.V_{t-1}, then rescale
+                    // O holds tiles 0..t-1 at the old maximum: wait for P_{t-1}.V_{t-1}, then rescale
                     if (!flags[0] && !mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit)) {
                         tc_report(p.err, WM_DEVERR_TIMEOUT);
                         flags[0] = 1;
                     }
                     o_stable = true;
                     tc::fence_after_sync();
-                    if (!flags[0]) {
+                    if (!warp_aborted(flags)) {
 #pragma unroll
-                        for (int a = 0; a <= C::NOC; ++a) {
-                            const uint32_t col = (a < C::NOC ? C::O_COL + a * NR : C::L_COL) + r0;
+                        for (int a = 0; a < C::NOC; ++a) {
+                            const uint32_t col = C::O_COL + a * NR + r0;
 #pragma unroll
                             for (int c = 0; c < HR / 8; ++c) {
                                 float v8[8];
@@ -474,6 +521,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float ma = m_run[i] == -CUDART_INF_F ? 0.f : m_run[i];
                 const float mb = m_run[i + 1] == -CUDART_INF_F ? 0.f : m_run[i + 1];
                 const float pa = ex2(s[i] - ma), pb = ex2(s[i + 1] - mb);
+                l_run[i] += pa;
+                l_run[i + 1] += pb;
                 const __nv_bfloat162 h = __floats2bfloat162_rn(pa, pb);
                 const __nv_bfloat162 l = __floats2bfloat162_rn(pa - __low2float(h), pb - __high2float(h));
                 hi_w[i / 2] = *reinterpret_cast<const uint32_t *>(&h);
@@ -488,16 +537,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t pt = sPT + (t % NPB) * 2 * C::PT_BYTES;
 #pragma unroll
             for (int j = 0; j < HR / 8; ++j) {
+                // MN-major P^T: key kt's row of PT_ROW bytes, 16-byte chunks of
+                // 8 rows permuted by the 128B (chunk ^ kt%8) or 64B
+                // (chunk ^ (kt/2)%4) swizzle
                 const int chunk = r0 / 8 + j;
-                const uint32_t off = (uint32_t)kt * 128u + ((uint32_t)(chunk ^ (kt & 7)) << 4);
+                const uint32_t phys = C::PT_ROW == 128 ? (uint32_t)(chunk ^ (kt & 7))
+                                                       : (uint32_t)(chunk ^ ((kt >> 1) & 3));
+                const uint32_t off = (uint32_t)kt * C::PT_ROW + (phys << 4);
                 st_shared_v4(pt + off, make_uint4(hi_w[4 * j], hi_w[4 * j + 1], hi_w[4 * j + 2], hi_w[4 * j + 3]));
                 st_shared_v4(pt + C::PT_BYTES + off,
                              make_uint4(lo_w[4 * j], lo_w[4 * j + 1], lo_w[4 * j + 2], lo_w[4 * j + 3]));
             }
             if (!key_ok && r0 == 0 && !flags[0]) {
-                // a key no row may see: zero its V row once the V tile has landed
+                // A key no row may see: zero its V row once the V tile has landed.
+                // The slot's previous unit is older than tile t-1's V, so once
+                // P_{t-1}.V_{t-1} is complete that unit has landed too and the
+                // parity wait below cannot mistake it for this tile's V.
                 const int uv = 2 * t + 1, sv = uv % C::NSLOT;
-                if (mbar_wait_bounded(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1, kWaitLimit)) {
+                const bool prev_in =
+                    t == 0 || mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit);
+                if (prev_in && mbar_wait_bounded(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1, kWaitLimit)) {
                     const uint32_t vrow = sbase + sv * C::SLOT_BYTES;
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
@@ -522,17 +581,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             flags[0] = 1;
         }
         tc::fence_after_sync();
-        const bool have = n_tiles > 0 && !flags[0];
+        const bool have = n_tiles > 0 && !warp_aborted(flags);
         const float kLn2 = 0.693147180559945309f;
+        // row sums: over the 32 keys of this warp, then over the 4 lane quadrants
+        // (the barrier keeps slower warps' last reads of red[] ahead of these writes)
+        named_bar_sync(1, 32 * kTcSoftmaxWarps);
+#pragma unroll
+        for (int i = 0; i < HR; ++i) {
+            float l = l_run[i];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (lane == 0) red[NR * q4 + r0 + i] = l;
+        }
+        named_bar_sync(1, 32 * kTcSoftmaxWarps);
 #pragma unroll
         for (int c = 0; c < HR / 8; ++c) {
             float l8[8];
-            if (have) {
-                tc::ld_32x32b_x8(tmem + lane_off + C::L_COL + r0 + 8 * c, l8);
-                tc::wait_ld();
-            } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + 8 * c + i;
+                l8[i] = have ? red[r] + red[NR + r] + red[2 * NR + r] + red[3 * NR + r] : 0.f;
             }
 #pragma unroll
             for (int m = 0; m < C::NOC; ++m) {

@@ -18,7 +18,7 @@ from . import build as _build
 
 WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, WM_ERR_DEVICE_DATA = range(6)
 WM_OP_DRAFT, WM_OP_VERIFY = 0, 1
-DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout"}
+DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout", 4: "internal check"}
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
