@@ -39,7 +39,7 @@ METRIC = "decode-attn µs/step & HBM GB/s (% roofline): windowed draft vs full v
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
-KERNEL_SOURCES = ("attn_kernel.cuh", "ptx.cuh", "wm_internal.h")
+KERNEL_SOURCES = ("attn_tc.cuh", "tc.cuh", "ptx.cuh", "wm_internal.h")
 
 
 def parse():
@@ -367,7 +367,7 @@ def gpu_arm(args, rank, world, local):
             "steps_per_s_all_ranks": round(world * 1e6 / us_step, 1),
         },
         "roofline": {
-            "kernel": "attn_kernel (verify, split-KV) + lse_merge",
+            "kernel": "attn_tc_kernel (tcgen05 verify, split-KV) + lse_merge",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -84,9 +84,13 @@ struct SplitPlan {
     int keys_per_split = 0;
 };
 
-// Keys per tile of the attention kernel that serves this head dim: the
-// tensor-core kernel (128) for 128 and 256, the mma.sync kernel (64) for 64.
-int key_tile(int head_dim) { return head_dim == 64 ? kKeyTile : kTcTile; }
+// Which attention kernel serves a call.  Verification at head dim 128/256 runs
+// on the tcgen05 kernel (128-key tiles, deep TMA staging, accumulators in
+// tensor memory): it streams gigabytes and is HBM-bound.  The draft reads a
+// few megabytes once per step; it is latency-bound, and the mma.sync kernel's
+// 64-key tiles give twice as many CTAs with a shorter fixed cost per CTA.
+bool use_tc_kernel(int op, int head_dim) { return op == WM_OP_VERIFY && head_dim != 64; }
+int key_tile(int op, int head_dim) { return use_tc_kernel(op, head_dim) ? kTcTile : kKeyTile; }
 
 // K+V bytes per split when a batch may be ragged (see plan_splits).
 constexpr int64_t kRaggedSplitBytes = 8ll << 20;
@@ -122,12 +126,17 @@ size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
     return o_aligned + (size_t)rows_total * n_split * sizeof(float);
 }
 
-cudaError_t launch_attn_any(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, cudaStream_t st) {
+cudaError_t launch_attn_any(int op, const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+                            cudaStream_t st) {
     const int m_tiles = (p.rows + 15) / 16;
+    if (use_tc_kernel(op, p.head_dim)) {
+        return p.head_dim == 128 ? launch_attn_tc_d128(k, v, p, 16 * m_tiles, st)
+                                 : launch_attn_tc_d256(k, v, p, 16 * m_tiles, st);
+    }
     switch (p.head_dim) {
         case 64: return launch_attn_d64(k, v, p, m_tiles, st);
-        case 128: return launch_attn_tc_d128(k, v, p, 16 * m_tiles, st);
-        case 256: return launch_attn_tc_d256(k, v, p, 16 * m_tiles, st);
+        case 128: return launch_attn_d128(k, v, p, m_tiles, st);
+        case 256: return launch_attn_d256(k, v, p, m_tiles, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -185,7 +194,7 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
     if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY) || batch <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 ||
         n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
         return 0;
-    return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(head_dim), head_dim).n_split;
+    return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim).n_split;
 }
 
 size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
@@ -264,11 +273,11 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
 
 // Shared tail of the two attention entry points: plan, check the workspace,
 // launch the attention kernel and (if split) the merge.
-static wm_status run_attention(AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv, int64_t max_keys,
-                               int32_t n_split, void *out, float *lse, void *ws, size_t ws_bytes,
-                               cudaStream_t st) {
+static wm_status run_attention(int op, AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                               int64_t max_keys, int32_t n_split, void *out, float *lse, void *ws,
+                               size_t ws_bytes, cudaStream_t st) {
     const SplitPlan pl =
-        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(p.head_dim), p.head_dim);
+        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim), p.head_dim);
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
     p.n_split = pl.n_split;
     p.keys_per_split = pl.keys_per_split;
@@ -283,7 +292,7 @@ static wm_status run_attention(AttnParams &p, const CUtensorMap &mk, const CUten
         p.o_part = static_cast<float *>(ws);
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + ((o + 255) & ~(size_t)255));
     }
-    cudaError_t e = launch_attn_any(mk, mv, p, st);
+    cudaError_t e = launch_attn_any(op, mk, mv, p, st);
     if (e != cudaSuccess) return WM_ERR_CUDA;
     if (pl.n_split > 1) {
         e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, st);
@@ -303,7 +312,7 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
     int32_t *err = device_error_ptr();
     if (!err) return WM_ERR_CUDA;
     const int n_slots = ring->sink + ring->window;
-    const int box = key_tile(ring->head_dim);
+    const int box = key_tile(WM_OP_DRAFT, ring->head_dim);
     CUtensorMap mk, mv;
     if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box) ||
         !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box))
@@ -328,7 +337,7 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
     p.rows = group;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.err = err;
-    return run_attention(p, mk, mv, n_slots, n_split, out, lse, workspace, workspace_bytes,
+    return run_attention(WM_OP_DRAFT, p, mk, mv, n_slots, n_split, out, lse, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
 }
 
@@ -350,7 +359,7 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     CUtensorMap mk, mv;
     const int64_t inner = paged ? kv->page_size : kv->n_cap;
     const int64_t outer = paged ? kv->n_pages : kv->batch;
-    const int tile = key_tile(kv->head_dim);
+    const int tile = key_tile(WM_OP_VERIFY, kv->head_dim);
     const int box = paged && kv->page_size % tile ? kKeyTile : tile;  // a box never crosses a page
     if (!encode_kv_map(&mk, kv->k, kv->head_dim, inner, kv->n_kv_heads, outer, box) ||
         !encode_kv_map(&mv, kv->v, kv->head_dim, inner, kv->n_kv_heads, outer, box))
@@ -375,7 +384,7 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     p.rows = group * n_q;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.err = err;
-    return run_attention(p, mk, mv, capacity, n_split, out, lse, workspace, workspace_bytes,
+    return run_attention(WM_OP_VERIFY, p, mk, mv, capacity, n_split, out, lse, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
 }
 

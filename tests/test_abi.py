@@ -116,9 +116,11 @@ def test_workspace_size_with_explicit_splits(lib):
     o = rows * ns * D * 4
     assert wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, ns) == \
         ((o + 255) // 256) * 256 + rows * ns * 4
-    # capped at one key tile per split: 128-key tiles (tensor-core kernel) for D=256, 64 for D=64
-    assert wm.plan_splits(wm.WM_OP_DRAFT, 1, 2, 16, 1, 256, 4100, 1000) == 33
-    assert wm.plan_splits(wm.WM_OP_DRAFT, 1, 2, 16, 1, 64, 4100, 1000) == 65
+    # capped at one key tile per split: the draft kernel's 64-key tiles, the
+    # verify kernel's 128-key tiles (tensor-core kernel) at head_dim 128/256
+    assert wm.plan_splits(wm.WM_OP_DRAFT, 1, 2, 16, 1, 256, 4100, 1000) == 65
+    assert wm.plan_splits(wm.WM_OP_VERIFY, 1, 2, 16, 1, 256, 4100, 1000) == 33
+    assert wm.plan_splits(wm.WM_OP_VERIFY, 1, 2, 16, 1, 64, 4100, 1000) == 65
     with pytest.raises(wm.WmError):
         wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 96, 1 << 20, 0)
 
