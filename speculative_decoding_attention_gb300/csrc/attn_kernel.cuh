@@ -232,8 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) oacc[m][n][e] = 0.f;
     }
     const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
+    // Ring slot tags this thread needs for one tile: the four keys of its S
+    // fragment and (lanes < 16) the key it checks for V-row zeroing.  They are
+    // fetched one tile ahead so that their latency hides behind the tile.
+    auto fetch_tags = [&](int64_t key0, int32_t(&tg)[2][2], int32_t &tg1) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
+                tg[n][e] = (tags && kabs < k_end) ? __ldg(tags + kabs) : -1;
+            }
+        const int64_t kl = key0 + warp * C::KPW + lane;
+        tg1 = (tags && lane < C::KPW && kl < k_end) ? __ldg(tags + kl) : -1;
+    };
+    auto tag_ok = [&](int64_t tg) {
+        return tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
+    };
+    int32_t tg_cur[2][2], tg1_cur, tg_nxt[2][2], tg1_nxt;
+    if (tags && n_tiles > 0) fetch_tags(k_begin, tg_cur, tg1_cur);
 
     for (int t = 0; t < n_tiles; ++t) {
+        if (tags && t + 1 < n_tiles) fetch_tags(k_begin + (int64_t)(t + 1) * TK, tg_nxt, tg1_nxt);
         const int s = t % C::STAGES;
         const int buf = t & 1;
         if (!*abort_flag && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, kWaitLimit)) {
@@ -285,10 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
                 bool ok = kabs < k_end;
-                if (ok && tags) {
-                    const int64_t tg = tags[kabs];
-                    ok = tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
-                }
+                if (ok && tags) ok = tag_ok(tg_cur[n][e]);
                 key_ok[n][e] = ok;
             }
 #pragma unroll
@@ -320,10 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < C::KPW) {
                 const int64_t kabs = key0 + warp * C::KPW + lane;
                 ok_all = kabs < k_end;
-                if (ok_all && tags) {
-                    const int64_t tg = tags[kabs];
-                    ok_all = tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
-                }
+                if (ok_all && tags) ok_all = tag_ok(tg1_cur);
             }
             uint32_t bad = ~__ballot_sync(0xffffffffu, ok_all) & ((1u << C::KPW) - 1u);
             if (bad) {
@@ -421,6 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (tags) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) tg_cur[n][e] = tg_nxt[n][e];
+            tg1_cur = tg1_nxt;
+        }
     }
 
     // ---- row sums across lanes and warps, normalise, write

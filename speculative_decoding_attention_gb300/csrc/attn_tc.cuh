@@ -12,14 +12,14 @@
 // kept per key-thread in registers and reduced once at the end.  The shared
 // memory split between K/V staging slots and P^T buffers is chosen per head
 // dim and row count: as many staging slots as fit, then a second P^T buffer
-// if it still fits.  Warp roles (10 warps):
+// if it still fits.  Warp roles (2 + 4g warps, g = max(2, NR / 16)):
 //   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
 //               shared-memory slots, K_t then V_t;
 //   warp 1    : allocates tensor memory; one lane issues whichever MMA is ready
 //               (S for the next tile, or P.V for the oldest tile whose P is
 //               written) and commits it to mbarriers;
-//   warps 2-9 : softmax -- one key per thread (a tensor-memory lane), two warps
-//               per lane quadrant each owning half of the rows: scale and mask
+//   warps 2.. : softmax -- one key per thread (a tensor-memory lane), g warps
+//               per lane quadrant each owning NR / g rows: scale and mask
 //               the logits, keep a running row maximum that is raised (with a
 //               rescale of O and L) only when a logit exceeds it by more than
 //               2^8, write P^T to shared memory as two bf16 parts
@@ -46,8 +46,10 @@
 namespace wm {
 
 constexpr int kTcKeyTile = 128;
-constexpr int kTcSoftmaxWarps = 8;
-constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+// Softmax warps for NR rows: groups of four (one per tensor-memory lane
+// quadrant), each group owning at most 16 rows (at least two groups).
+__host__ __device__ constexpr int tc_softmax_warps(int nr) { return 4 * (nr / 16 < 2 ? 2 : nr / 16); }
+__host__ __device__ constexpr int tc_threads(int nr) { return (2 + tc_softmax_warps(nr)) * 32; }
 constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
 
 template <int D, int NR, int NSLOT_, int NPB_>
@@ -66,8 +68,8 @@ struct TcLayout {
     static constexpr int PT_OFF = Q_OFF + NCH * Q_REGION;      // NPB x (P^T hi, P^T lo)
     static constexpr int PT_BYTES = TK * PT_ROW;
     static constexpr int RED_OFF = PT_OFF + 2 * NPB * PT_BYTES;  // float red[4][NR]
-    static constexpr int FLAG_OFF = RED_OFF + 4 * NR * 4;        // int flags[32]
-    static constexpr int BAR_OFF = FLAG_OFF + 128;
+    static constexpr int FLAG_OFF = RED_OFF + 4 * NR * 4;        // int flags[64]
+    static constexpr int BAR_OFF = FLAG_OFF + 256;
     static constexpr int NBAR = 2 * NSLOT + 10;
     static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = TPTR_OFF + 16 + 1024;
@@ -94,7 +96,9 @@ struct TcCfg {
     static constexpr int Q_OFF = L::Q_OFF, Q_REGION = L::Q_REGION, PT_OFF = L::PT_OFF, PT_BYTES = L::PT_BYTES;
     static constexpr int RED_OFF = L::RED_OFF;
     static constexpr int FLAG_OFF = L::FLAG_OFF, BAR_OFF = L::BAR_OFF, TPTR_OFF = L::TPTR_OFF, TOTAL = L::TOTAL;
-    static constexpr int HR = NR / 2;                          // rows per softmax half
+    static constexpr int NSW = tc_softmax_warps(NR);            // softmax warps
+    static constexpr int THREADS = tc_threads(NR);
+    static constexpr int HR = NR / (NSW / 4);                  // rows per softmax warp
     static constexpr int S_COL = 0;                            // 2 x NR
     static constexpr int O_COL = 2 * NR;                       // NOC x NR
     static constexpr int TMEM_USED = O_COL + NOC * NR;
@@ -121,12 +125,14 @@ __device__ __forceinline__ bool in_smem(uint32_t lo, uint32_t len, uint32_t base
 }
 
 template <int D, int NR>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads(NR), 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const AttnParams p) {
     using C = TcCfg<D, NR>;
     constexpr int TK = C::TK;
     constexpr int HR = C::HR;
+    constexpr int NSW = C::NSW;
+    constexpr int kTcThreads = C::THREADS;
     constexpr int NPB = C::NPB;
 
     extern __shared__ uint8_t smem_raw[];
@@ -203,13 +209,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull + 8 * i, 1);
-            mbar_init(bar_sfree + 8 * i, kTcSoftmaxWarps);
-            mbar_init(bar_pfull + 8 * i, kTcSoftmaxWarps);
+            mbar_init(bar_sfree + 8 * i, NSW);
+            mbar_init(bar_pfull + 8 * i, NSW);
             mbar_init(bar_odone + 8 * i, 1);
         }
-        mbar_init(bar_qfull, kTcSoftmaxWarps);
+        mbar_init(bar_qfull, NSW);
         mbar_init(bar_final, 1);
-        for (int i = 0; i < 32; ++i) flags[i] = 0;
+        for (int i = 0; i < 64; ++i) flags[i] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -383,16 +389,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ======================================================== softmax warps
-        const int sw = warp - 2;                       // 0..7
+        const int sw = warp - 2;                       // 0..NSW-1
         const int q4 = warp & 3;                       // tensor-memory lane quadrant
-        const int r0 = (sw >> 2) * HR;                 // first row of this warp's half
+        const int r0 = (sw >> 2) * HR;                 // first row of this warp's group
         const int kt = 32 * q4 + lane;                 // key within the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        const int ct = threadIdx.x - 64;               // 0..255
+        const int ct = threadIdx.x - 64;               // 0..32*NSW-1
         {
             const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
             constexpr int VPR = D / 8;
-            for (int idx = ct; idx < NR * VPR; idx += 32 * kTcSoftmaxWarps) {
+            for (int idx = ct; idx < NR * VPR; idx += 32 * NSW) {
                 const int r = idx / VPR, v = idx - (idx / VPR) * VPR;
                 uint4 val = make_uint4(0u, 0u, 0u, 0u);
                 if (r < p.rows) {
@@ -458,11 +464,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 need |= v > m_run[i] + kLazyRescale;
             }
             const unsigned any = __ballot_sync(0xffffffffu, need);
-            if (lane == 0) flags[8 + 8 * (t & 1) + sw] = any != 0u;
-            named_bar_sync(1, 32 * kTcSoftmaxWarps);
+            if (lane == 0) flags[8 + 16 * (t & 1) + sw] = any != 0u;
+            named_bar_sync(1, 32 * NSW);
             int votes = 0;
 #pragma unroll
-            for (int w = 0; w < kTcSoftmaxWarps; ++w) votes |= flags[8 + 8 * (t & 1) + w];
+            for (int w = 0; w < NSW; ++w) votes |= flags[8 + 16 * (t & 1) + w];
             const bool rescale = votes != 0;
             if (rescale) {
 #pragma unroll
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) red[NR * q4 + r0 + i] = mx;
                 }
             }
-            named_bar_sync(1, 32 * kTcSoftmaxWarps);
+            named_bar_sync(1, 32 * NSW);
             bool o_stable = t == 0;  // P_{t-1}.V_{t-1} known complete
             if (rescale) {
                 float alpha[HR];
@@ -585,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float kLn2 = 0.693147180559945309f;
         // row sums: over the 32 keys of this warp, then over the 4 lane quadrants
         // (the barrier keeps slower warps' last reads of red[] ahead of these writes)
-        named_bar_sync(1, 32 * kTcSoftmaxWarps);
+        named_bar_sync(1, 32 * NSW);
 #pragma unroll
         for (int i = 0; i < HR; ++i) {
             float l = l_run[i];
@@ -593,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
             if (lane == 0) red[NR * q4 + r0 + i] = l;
         }
-        named_bar_sync(1, 32 * kTcSoftmaxWarps);
+        named_bar_sync(1, 32 * NSW);
 #pragma unroll
         for (int c = 0; c < HR / 8; ++c) {
             float l8[8];
@@ -667,7 +673,7 @@ cudaError_t launch_attn_tc_nr(const CUtensorMap &k, const CUtensorMap &v, const 
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    return launch_pdl(attn_tc_kernel<D, NR>, grid, dim3(kTcThreads), smem, stream, k, v, p);
+    return launch_pdl(attn_tc_kernel<D, NR>, grid, dim3(TcCfg<D, NR>::THREADS), smem, stream, k, v, p);
 }
 
 template <int D>
