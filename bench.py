@@ -310,6 +310,7 @@ def gpu_arm(args, rank, world, local):
     if wm.get_device_error():
         raise RuntimeError("device error during the timed steps")
     out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
+    native_ms = native_draft_chain(st, flush, args)
 
     us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
     us_verify = 1e3 * sum(verify_ms) / len(verify_ms)
@@ -365,6 +366,11 @@ def gpu_arm(args, rank, world, local):
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
             "outputs_finite": out_ok,
             "steps_per_s_all_ranks": round(world * 1e6 / us_step, 1),
+            "native_draft_chain_us": round(1e3 * native_ms, 2),
+            "native_draft_us_per_step": round(1e3 * native_ms / depth, 2),
+            "native_step_us": None if us_draft is None else round(us_step - us_draft + 1e3 * native_ms, 2),
+            "native_over_windowed_step": None if us_draft is None else
+            round((us_step - us_draft + 1e3 * native_ms) / us_step, 3),
         },
         "roofline": {
             "kernel": "attn_tc_kernel (tcgen05 verify, split-KV) + lse_merge",
@@ -382,6 +388,47 @@ def gpu_arm(args, rank, world, local):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def native_draft_chain(st: Step, flush, args) -> float:
+    """The draft chain without windowing (the native MTP draft the pages compare
+    against): each of the d draft steps attends over the whole cache, i.e. the
+    verify kernel with one query position over positions 0..N_b+j.  Returns the
+    mean milliseconds per chain (graph-captured, L2 flushed between chains)."""
+    wm, w, inp = st.wm, st.w, st.inp
+    B, Hq, D = w.batch, w.n_q_heads, w.head_dim
+    lens = [torch.tensor([n + j + 1 for n in inp.seq_lens_host], dtype=torch.int64, device=st.dev)
+            for j in range(st.d)]
+    kvs = [wm.KVCache(inp.k, inp.v, lens[j], inp.block_table) for j in range(st.d)]
+    qs = [inp.q_draft[j].view(B, 1, Hq, D) for j in range(st.d)]
+    out = torch.empty((B, 1, Hq, D), dtype=torch.bfloat16, device=st.dev)
+    lse = torch.empty((B, 1, Hq), dtype=torch.float32, device=st.dev)
+    need = wm.workspace_size(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, 1, D, st.kv.capacity)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=st.dev)
+
+    def chain():
+        for j in range(st.d):
+            wm.verify_attn(kvs[j], qs[j], w.scale, out=out, lse=lse, workspace=ws)
+
+    chain()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=st.dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ms = []
+    for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
+        flush.zero_()
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        if i >= max(3, args.warmup):
+            ms.append(e0.elapsed_time(e1))
+    return sum(ms) / len(ms)
 
 
 def e2e_leg(st: Step, args, world, device) -> dict:

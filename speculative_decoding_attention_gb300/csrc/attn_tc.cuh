@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             int votes = 0;
 #pragma unroll
             for (int w = 0; w < NSW; ++w) votes |= flags[8 + 16 * (t & 1) + w];
-            const bool rescale = votes != 0;
+            const bool rescale = votes != 0;  // the same in every softmax thread
             if (rescale) {
 #pragma unroll
                 for (int i = 0; i < HR; ++i) {
@@ -478,8 +478,8 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
                     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                     if (lane == 0) red[NR * q4 + r0 + i] = mx;
                 }
+                named_bar_sync(1, 32 * NSW);
             }
-            named_bar_sync(1, 32 * NSW);
             bool o_stable = t == 0;  // P_{t-1}.V_{t-1} known complete
             if (rescale) {
                 float alpha[HR];
