@@ -12,7 +12,7 @@
 // kept per key-thread in registers and reduced once at the end.  The shared
 // memory split between K/V staging slots and P^T buffers is chosen per head
 // dim and row count: as many staging slots as fit, then a second P^T buffer
-// if it still fits.  Warp roles (2 + 4g warps, g = max(2, NR / 16)):
+// if it still fits.  Warp roles (2 + 4g warps, g = NR / 8 up to 32 rows, else NR / 16):
 //   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
 //               shared-memory slots, K_t then V_t;
 //   warp 1    : allocates tensor memory; one lane issues whichever MMA is ready
@@ -46,9 +46,12 @@
 namespace wm {
 
 constexpr int kTcKeyTile = 128;
+constexpr int kTcPageCache = 256;  // block-table entries of one split kept in shared memory
 // Softmax warps for NR rows: groups of four (one per tensor-memory lane
-// quadrant), each group owning at most 16 rows (at least two groups).
-__host__ __device__ constexpr int tc_softmax_warps(int nr) { return 4 * (nr / 16 < 2 ? 2 : nr / 16); }
+// quadrant), each group owning 8 rows up to 32 rows and 16 rows beyond (more
+// warps would leave too few registers per thread).  More, shorter softmax
+// warps hide the latency of the tensor-memory loads, MUFU and barriers per tile.
+__host__ __device__ constexpr int tc_softmax_warps(int nr) { return nr <= 32 ? 4 * (nr / 8) : 4 * (nr / 16); }
 __host__ __device__ constexpr int tc_threads(int nr) { return (2 + tc_softmax_warps(nr)) * 32; }
 constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
 
@@ -69,20 +72,23 @@ struct TcLayout {
     static constexpr int PT_BYTES = TK * PT_ROW;
     static constexpr int RED_OFF = PT_OFF + 2 * NPB * PT_BYTES;  // float red[4][NR]
     static constexpr int FLAG_OFF = RED_OFF + 4 * NR * 4;        // int flags[64]
-    static constexpr int BAR_OFF = FLAG_OFF + 256;
+    static constexpr int BT_OFF = FLAG_OFF + 256;                // int page_cache[kTcPageCache]
+    static constexpr int BAR_OFF = BT_OFF + 4 * kTcPageCache;
     static constexpr int NBAR = 2 * NSLOT + 10;
     static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = TPTR_OFF + 16 + 1024;
     static constexpr bool FITS = TOTAL <= 227 * 1024;
 };
 
-// Shared-memory plan: the most K/V staging slots (up to 4) that fit with one
-// P^T buffer -- keeping HBM requests in flight matters most, and 3 slots
-// already let the next tile's K and V load while this tile computes -- then a
-// second P^T buffer if it fits too.
+// Shared-memory plan: the most K/V staging slots (up to 6) that fit with one
+// P^T buffer -- keeping enough HBM requests in flight per SM (well over 100 KB
+// at loaded HBM latency) matters most -- then a second P^T buffer if it fits.
 template <int D, int NR>
 struct TcPlan {
-    static constexpr int NSLOT = TcLayout<D, NR, 4, 1>::FITS ? 4 : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
+    static constexpr int NSLOT = TcLayout<D, NR, 6, 1>::FITS   ? 6
+                                 : TcLayout<D, NR, 5, 1>::FITS ? 5
+                                 : TcLayout<D, NR, 4, 1>::FITS ? 4
+                                 : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
     static constexpr int NPB = TcLayout<D, NR, NSLOT, 2>::FITS ? 2 : 1;
 };
 
@@ -96,6 +102,7 @@ struct TcCfg {
     static constexpr int Q_OFF = L::Q_OFF, Q_REGION = L::Q_REGION, PT_OFF = L::PT_OFF, PT_BYTES = L::PT_BYTES;
     static constexpr int RED_OFF = L::RED_OFF;
     static constexpr int FLAG_OFF = L::FLAG_OFF, BAR_OFF = L::BAR_OFF, TPTR_OFF = L::TPTR_OFF, TOTAL = L::TOTAL;
+    static constexpr int BT_OFF = L::BT_OFF;
     static constexpr int NSW = tc_softmax_warps(NR);            // softmax warps
     static constexpr int THREADS = tc_threads(NR);
     static constexpr int HR = NR / (NSW / 4);                  // rows per softmax warp
@@ -229,6 +236,24 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
 
     if (warp == 0) {
         // ======================================================== TMA producer
+        // Paged caches: the whole warp first copies this split's block-table
+        // entries into shared memory, so that the lane issuing the copies never
+        // waits on a global load per box (entries past the cache are read from
+        // global memory as they are needed).
+        int32_t *page_cache = reinterpret_cast<int32_t *>(gb + C::BT_OFF);
+        const int64_t first_page = p.source == KEYS_PAGED ? k_begin / p.page_size : 0;
+        if (p.source == KEYS_PAGED) {
+            const int64_t n_pages_split = (k_end - 1) / p.page_size - first_page + 1;
+            for (int i = lane; i < kTcPageCache && i < n_pages_split; i += 32) {
+                int32_t page = p.block_table[(int64_t)b * p.max_pages + first_page + i];
+                if (page < 0 || page >= p.n_pages) {
+                    tc_report(p.err, WM_DEVERR_BAD_PAGE);
+                    page = 0;
+                }
+                page_cache[i] = page;
+            }
+            __syncwarp();
+        }
         if (lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
@@ -254,10 +279,16 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
                     int c_row, c_outer;
                     if (p.source == KEYS_PAGED) {
                         if (kh < n_keys) {
-                            int32_t page = p.block_table[(int64_t)b * p.max_pages + kh / p.page_size];
-                            if (page < 0 || page >= p.n_pages) {
-                                tc_report(p.err, WM_DEVERR_BAD_PAGE);
-                                page = 0;
+                            const int64_t local = kh / p.page_size - first_page;
+                            int32_t page;
+                            if (local < kTcPageCache) {
+                                page = page_cache[local];
+                            } else {
+                                page = p.block_table[(int64_t)b * p.max_pages + kh / p.page_size];
+                                if (page < 0 || page >= p.n_pages) {
+                                    tc_report(p.err, WM_DEVERR_BAD_PAGE);
+                                    page = 0;
+                                }
                             }
                             last_page = page;
                         }
