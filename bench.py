@@ -199,11 +199,12 @@ class Step:
         self.d_lse = torch.empty((depth, B, Hq), dtype=torch.float32, device=device)
         self.v_out = torch.empty_like(inp.q_verify)
         self.v_lse = torch.empty(inp.q_verify.shape[:3], dtype=torch.float32, device=device)
-        self.d_splits = wm.plan_splits(wm.WM_OP_DRAFT, B, w.n_kv_heads, Hq, 1, D, w.slots)
+        self.d_splits = wm.plan_splits(wm.WM_OP_DRAFT_STEP, B, w.n_kv_heads, Hq, 1, D, w.slots)
         self.v_splits = wm.plan_splits(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
         dws = wm.workspace_size(wm.WM_OP_DRAFT, B, w.n_kv_heads, Hq, 1, D, w.slots)
         vws = wm.workspace_size(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
         self.d_ws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
+        self.s_ws = wm.step_workspace(self.ring, Hq)  # the fused step's own (zeroed) workspace
         self.v_ws = torch.empty(max(vws, 256), dtype=torch.uint8, device=device)
         self.graph = None
         self.ev = None
@@ -220,18 +221,29 @@ class Step:
         else:
             wm.ring_fill(self.ring, self.kv)
 
-    def launches_per_step(self) -> int:
-        per_draft = 2 + (1 if self.d_splits > 1 else 0)
+    def launches_per_step(self, fused: bool = True) -> int:
+        per_draft = 2 if fused else 2 + (1 if self.d_splits > 1 else 0)
         return self.d * per_draft + 1 + (1 if self.v_splits > 1 else 0) + 1
 
-    def run(self, ev=None):
+    def draft(self, j: int, fused: bool = True, q=None, k_new=None, v_new=None):
+        """Draft step j: the fused step (append in the attention launch, then the merge), or ring
+        append + draft attention (+ merge)."""
+        wm, w, inp = self.wm, self.w, self.inp
+        q = inp.q_draft[j] if q is None else q
+        k_new = inp.k_new[j] if k_new is None else k_new
+        v_new = inp.v_new[j] if v_new is None else v_new
+        if fused:
+            wm.draft_step(self.ring, k_new, v_new, q, w.scale, self.s_ws, out=self.d_out[j], lse=self.d_lse[j])
+        else:
+            wm.ring_append(self.ring, k_new, v_new)
+            wm.draft_attn(self.ring, q, w.scale, out=self.d_out[j], lse=self.d_lse[j], workspace=self.d_ws)
+
+    def run(self, ev=None, fused: bool = True):
         wm, w, inp = self.wm, self.w, self.inp
         if ev:
             ev[0].record()
         for j in range(self.d):
-            wm.ring_append(self.ring, inp.k_new[j], inp.v_new[j])
-            wm.draft_attn(self.ring, inp.q_draft[j], w.scale, out=self.d_out[j], lse=self.d_lse[j],
-                          workspace=self.d_ws)
+            self.draft(j, fused)
         if ev:
             ev[1].record()
         wm.verify_attn(self.kv, inp.q_verify, w.scale, out=self.v_out, lse=self.v_lse, workspace=self.v_ws)
@@ -239,19 +251,22 @@ class Step:
             ev[2].record()
         wm.ring_rollback(self.ring, self.base_len)
 
-    def capture(self):
-        self.run()  # eager once: kernel attributes, descriptors, first-touch
+    def capture(self, fused: bool = True):
+        """Capture one step in a CUDA graph; returns (graph, in-graph events or None)."""
+        self.run(fused=fused)  # eager once: kernel attributes, descriptors, first-touch
         torch.cuda.synchronize()
         try:
-            self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
         except TypeError:
-            self.ev = None
+            ev = None
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream())
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=s):
-            self.run(self.ev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            self.run(ev, fused=fused)
         torch.cuda.synchronize()
+        self.graph, self.ev = graph, ev
+        return graph, ev
 
 
 def gpu_arm(args, rank, world, local):
@@ -311,6 +326,7 @@ def gpu_arm(args, rank, world, local):
         raise RuntimeError("device error during the timed steps")
     out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
     native_ms = native_draft_chain(st, flush, args)
+    unfused_ms = unfused_draft_chain(st, flush, args)
 
     us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
     us_verify = 1e3 * sum(verify_ms) / len(verify_ms)
@@ -353,6 +369,8 @@ def gpu_arm(args, rank, world, local):
             "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D, "sink": w.sink, "window": w.window,
             "draft_depth": depth, "verify_positions": st.T, "kv_layout": "paged" if w.page_size else "contiguous",
             "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+            "draft_execution": "per draft step: one launch of ring append fused into the draft attention, "
+                               "then the split merge (which commits the append)",
             "l2": "flushed between timed steps (write of 2x L2); each step also reads the full KV cache (> L2)",
             "execution": "one CUDA graph per step", "parallelism": f"replicas x{world}",
         },
@@ -362,7 +380,11 @@ def gpu_arm(args, rank, world, local):
             "draft_chain_us": None if us_draft is None else round(us_draft, 2),
             "draft_us_per_step": None if us_draft is None else round(us_draft / depth, 2),
             "draft_gbs": None if draft_gbs is None else round(draft_gbs, 1),
+            "draft_frac_of_hbm": None if draft_gbs is None else round(draft_gbs / peak, 4),
             "draft_kv_bytes_per_step": 2 * B * Hkv * w.slots * D * 2,
+            "draft_l2": "L2 flushed before each step; draft steps 2..d re-read the ring (S+W slots) "
+                        "mostly from L2, as a decode loop does",
+            "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
             "outputs_finite": out_ok,
             "steps_per_s_all_ranks": round(world * 1e6 / us_step, 1),
@@ -388,6 +410,23 @@ def gpu_arm(args, rank, world, local):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def unfused_draft_chain(st: Step, flush, args):
+    """The draft chain as three launches per draft step (ring append, draft
+    attention, split merge): the whole step captured with in-graph events,
+    the draft interval averaged.  None without in-graph events."""
+    graph, ev = st.capture(fused=False)
+    if not ev:
+        return None
+    ms = []
+    for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
+        flush.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        if i >= max(3, args.warmup):
+            ms.append(ev[0].elapsed_time(ev[1]))
+    return sum(ms) / len(ms)
 
 
 def native_draft_chain(st: Step, flush, args) -> float:
@@ -463,9 +502,7 @@ def e2e_leg(st: Step, args, world, device) -> dict:
                 inp.k[b, :, n - T:n].copy_(dev_in["k_tail"][b])
                 inp.v[b, :, n - T:n].copy_(dev_in["v_tail"][b])
         for j in range(st.d):
-            wm.ring_append(st.ring, dev_in["k_new"][j], dev_in["v_new"][j])
-            wm.draft_attn(st.ring, dev_in["q_draft"][j], w.scale, out=st.d_out[j], lse=st.d_lse[j],
-                          workspace=st.d_ws)
+            st.draft(j, True, q=dev_in["q_draft"][j], k_new=dev_in["k_new"][j], v_new=dev_in["v_new"][j])
         wm.verify_attn(st.kv, dev_in["q_verify"], w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
         wm.ring_rollback(st.ring, st.base_len)
         host_out["d_out"].copy_(st.d_out, non_blocking=True)

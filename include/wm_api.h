@@ -98,8 +98,7 @@ typedef struct wm_ring {
  *       k, v  [n_pages][n_kv_heads][page_size][head_dim] bf16
  *       block_table [batch][max_pages] int32: position j of sequence b lives
  *       in page block_table[b][j / page_size], row j % page_size.
- *       page_size must be a multiple of the key tile (64 keys for head_dim
- *       <= 128, 32 for head_dim 256).
+ *       page_size must be a multiple of 64 (whole 64-key boxes per page).
  *   seq_lens [batch] int64: number of valid positions of each sequence.
  * k and v must be 16-byte aligned.
  */
@@ -221,9 +220,39 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
 wm_status wm_draft_attn_static(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale,
                                int32_t n_split, void *out, float *lse, void *stream);
 
+/*
+ * Fused draft step: wm_ring_append followed by wm_draft_attn, with the append
+ * folded into the attention launch (one attention launch + one merge launch
+ * instead of append + attention (+ merge)).  The windowed draft reads only
+ * the sinks and the window (Abstract: the draft attends to a sliding window
+ * plus attention sinks held in a compact ring buffer), a few megabytes per
+ * step, so its cost is launch and latency bound and the separate append
+ * launch is a large part of it.  For each sequence b, with p = n_seen[b] on
+ * entry:
+ *   - the query q[b] sits at position p and attends to every ring slot whose
+ *     tag t satisfies 0 <= t <= p and (t < sink or t > p - window), where
+ *     slot(p) counts as holding p with K/V = k_new[b], v_new[b];
+ *   - on completion slot(p) holds k_new[b], v_new[b], pos_tag[b][slot(p)] = p
+ *     and n_seen[b] = p + 1 -- the state wm_ring_append leaves.
+ *   k_new, v_new  [batch][n_kv_heads][head_dim] bf16
+ *   q, out        [batch][n_q_heads][head_dim] bf16;  lse [batch][n_q_heads] fp32 or NULL
+ *   n_split       as for wm_draft_attn (same plan).
+ *   workspace     at least wm_workspace_size(WM_OP_DRAFT_STEP, batch, n_kv_heads,
+ *                 n_q_heads, 1, head_dim, sink + window, n_split) bytes (never 0:
+ *                 the split partials always pass through the merge, which
+ *                 commits n_seen), 256-byte aligned; no initial contents needed.
+ * out, lse and the ring are bit-identical to wm_ring_append + wm_draft_attn
+ * with the same n_split.  A negative n_seen[b] records WM_DEVERR_BAD_LENGTH,
+ * appends nothing for b and gives its rows out = 0, lse = -inf.
+ */
+wm_status wm_draft_step(const wm_ring *ring, const void *k_new, const void *v_new, const void *q,
+                        int32_t n_q_heads, float scale, int32_t n_split, void *out, float *lse,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Operations for wm_workspace_size / wm_plan_splits. */
 #define WM_OP_DRAFT 0
 #define WM_OP_VERIFY 1
+#define WM_OP_DRAFT_STEP 2
 
 /*
  * Number of key splits an attention call will use, for a cache holding up to
@@ -235,7 +264,8 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
 
 /*
  * Workspace bytes an attention call needs for the same arguments (0 when it
- * runs unsplit).  For WM_OP_DRAFT pass n_q = 1 and max_keys = sink + window;
+ * runs unsplit; never 0 for WM_OP_DRAFT_STEP).  For WM_OP_DRAFT and
+ * WM_OP_DRAFT_STEP pass n_q = 1 and max_keys = sink + window;
  * for WM_OP_VERIFY, max_keys = n_cap (contiguous) or max_pages * page_size.
  * Returns (size_t)-1 on invalid arguments.
  */

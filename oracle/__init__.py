@@ -151,6 +151,15 @@ def _rows(rows, total: int):
     return r, r.size
 
 
+def _check_batch(kv: KV, batch: int, n_pos: int, head_dim: int) -> None:
+    # The C routines index queries and positions by the store's batch: a query
+    # batch or position list of another size would be read or written out of
+    # bounds.
+    if batch != kv.c.batch or n_pos != batch or head_dim != kv.c.head_dim:
+        raise ValueError(f"query batch {batch} / positions {n_pos} / head_dim {head_dim} do not match "
+                         f"the store (batch {kv.c.batch}, head_dim {kv.c.head_dim})")
+
+
 def verify(kv: KV, q, seq_lens, scale: float, rows=None, plant: int = 0):
     """Full-context causal attention of the T proposed positions.
 
@@ -161,6 +170,7 @@ def verify(kv: KV, q, seq_lens, scale: float, rows=None, plant: int = 0):
     qb = _bits(q)
     B, T, Hq, D = qb.shape
     sl = _i64(seq_lens)
+    _check_batch(kv, B, sl.size, D)
     r, n = _rows(rows, B * T * Hq)
     out = np.zeros((n, D), np.float64)
     lse = np.zeros((n,), np.float64)
@@ -180,6 +190,7 @@ def draft(hist: KV, q, pos, sink: int, window: int, scale: float, rows=None, pla
     qb = _bits(q)
     B, Hq, D = qb.shape
     p = _i64(pos)
+    _check_batch(hist, B, p.size, D)
     r, n = _rows(rows, B * Hq)
     out = np.zeros((n, D), np.float64)
     lse = np.zeros((n,), np.float64)

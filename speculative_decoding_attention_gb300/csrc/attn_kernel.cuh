@@ -23,6 +23,16 @@
 // The split's normalised output and its log-sum-exp go either straight to the
 // bf16 output (one split) or to fp32 partials that a merge kernel combines.
 //
+// Fused draft step (STEP = true): ring append + draft attention in one
+// launch.  Every CTA reads p = n_seen[b] (the position being appended) and
+// treats ring slot(p) as holding p: the CTA whose key range contains that slot
+// copies the new K/V row over the stale one in its staged tile (its TMA read
+// the ring before the append) and stores the row and its tag into the ring.
+// The split partials always go to the merge kernel, which also commits
+// n_seen[b] = p + 1 -- after this grid has finished, so no CTA can see the
+// new count early.  Same splits and merge as the unfused draft, so the outputs
+// are bit-identical to ring append + draft attention.
+//
 // Masks: verification is causal (query i sees positions <= seq_len - n_q + i);
 // the draft sees a ring slot iff its tag t satisfies 0 <= t <= p and
 // (t < sink or t > p - window).  Keys masked for every row get their V row
@@ -46,7 +56,7 @@ struct AttnCfg {
     static constexpr int NCH = D / 64;                           // 128-byte chunks per row
     static constexpr int TILE_BYTES = TK * D * 2;                // K (or V) tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int STAGES = kStagingBytes / STAGE_BYTES;   // 8 / 4 / 2
+    static constexpr int STAGES = staging_bytes(D) / STAGE_BYTES;  // 4 / 4 / 2
     static constexpr int NW = kConsumerWarps;
     static constexpr int KPW = TK / NW;                          // keys per warp in Q K^T
     static constexpr int DW = D / NW;                            // head-dim columns per warp in P V
@@ -66,9 +76,11 @@ struct AttnSmem {
     static constexpr int RED_BYTES = 3 * kConsumerWarps * ROWS * 4;
     static constexpr int BAR_OFF = RED_OFF + RED_BYTES;            // full[STAGES], empty[STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + 2 * AttnCfg<D>::STAGES * 8;
-    static constexpr int TOTAL = FLAG_OFF + 16 + 1024;             // + slack to 1024-align the base
+    static constexpr int NEW_OFF = FLAG_OFF + 16;                  // fused step: appended K and V rows
+    static constexpr int TOTAL = NEW_OFF + 2 * D * 2 + 1024;       // + slack to 1024-align the base
     static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && P_BYTES % 1024 == 0,
                   "swizzled regions need 1024-byte alignment");
+    static_assert(NEW_OFF % 16 == 0, "16-byte vectors");
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
@@ -76,7 +88,7 @@ __device__ __forceinline__ void report_error(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
 
-template <int D, int MT>
+template <int D, int MT, bool STEP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
@@ -109,14 +121,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- keys of this split, and the position of query 0
     int64_t n_keys, qpos0;
+    int64_t new_slot = -1;  // STEP: ring slot receiving position qpos0
     if (p.source == KEYS_RING) {
         int64_t seen = p.n_seen[b];
         if (seen < 0) {
             if (threadIdx.x == 0) report_error(p.err, WM_DEVERR_BAD_LENGTH);
-            seen = 0;
+            seen = STEP ? -1 : 0;  // STEP: nothing is appended, every key is masked
         }
         n_keys = p.n_slots;
-        qpos0 = seen - 1;
+        qpos0 = STEP ? seen : seen - 1;
+        if (STEP && seen >= 0) new_slot = seen < p.sink ? seen : p.sink + (seen - p.sink) % p.window;
     } else {
         int64_t len = p.seq_lens[b];
         if (len < 0 || len > p.capacity) {
@@ -145,7 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            const uint64_t policy = l2_policy_evict_first();
+            // The cache is streamed once per call; the ring is read again by the
+            // next draft step, so its lines keep normal priority.
+            const uint64_t policy =
+                p.source == KEYS_RING ? l2_policy_evict_normal() : l2_policy_evict_first();
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int s = t % C::STAGES;
@@ -191,6 +208,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // =========================================================== compute warps
     constexpr int NCT = C::NW * 32;  // compute threads
+    // STEP: the CTA whose keys include slot(p) stages the appended K row
+    // (threads 0..D/8-1) and V row (D/8..D/4-1) in shared memory with Q.
+    constexpr int NVR = D / 8;
+    const bool has_new = STEP && new_slot >= k_begin && new_slot < k_end;
+    uint4 *s_new = reinterpret_cast<uint4 *>(gbase + L::NEW_OFF);
+    if (has_new && threadIdx.x < 2 * NVR) {
+        const uint4 *src = static_cast<const uint4 *>(threadIdx.x < NVR ? p.k_new : p.v_new);
+        s_new[threadIdx.x] = __ldg(src + ((int64_t)b * p.n_kv_heads + kvh) * NVR + threadIdx.x % NVR);
+    }
     {
         const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
         constexpr int VPR = D / 8;  // 16-byte vectors per row
@@ -249,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tag_ok = [&](int64_t tg) {
         return tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
     };
+    // The tag a key is judged by: STEP's appended slot holds qpos0 already.
+    auto tag_of = [&](int64_t kabs, int32_t tg) -> int64_t {
+        return STEP && kabs == new_slot ? qpos0 : (int64_t)tg;
+    };
     int32_t tg_cur[2][2], tg1_cur, tg_nxt[2][2], tg1_nxt;
     if (tags && n_tiles > 0) fetch_tags(k_begin, tg_cur, tg1_cur);
 
@@ -264,6 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t key0 = k_begin + (int64_t)t * TK;
         const uint32_t sK = sbase + s * C::STAGE_BYTES;
         const uint32_t sV = sK + C::TILE_BYTES;
+
+        // ---- STEP: the appended K/V row replaces the ring's stale row
+        if (has_new && new_slot >= key0 && new_slot < key0 + TK) {
+            if (live && threadIdx.x < 2 * NVR) {
+                const int row = (int)(new_slot - key0), v = threadIdx.x % NVR;
+                st_shared_v4((threadIdx.x < NVR ? sK : sV) + (v >> 3) * (TK * 128) + swz128(row, v & 7),
+                             s_new[threadIdx.x]);
+                fence_proxy_async_smem();  // the stage is refilled by TMA later
+            }
+            named_bar_sync(1, NCT);
+        }
 
         // ---- S = Q K^T for this warp's 16 keys
         float sacc[MT][2][4];
@@ -305,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
                 bool ok = kabs < k_end;
-                if (ok && tags) ok = tag_ok(tg_cur[n][e]);
+                if (ok && tags) ok = tag_ok(tag_of(kabs, tg_cur[n][e]));
                 key_ok[n][e] = ok;
             }
 #pragma unroll
@@ -337,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < C::KPW) {
                 const int64_t kabs = key0 + warp * C::KPW + lane;
                 ok_all = kabs < k_end;
-                if (ok_all && tags) ok_all = tag_ok(tg1_cur);
+                if (ok_all && tags) ok_all = tag_ok(tag_of(kabs, tg1_cur));
             }
             uint32_t bad = ~__ballot_sync(0xffffffffu, ok_all) & ((1u << C::KPW) - 1u);
             if (bad) {
@@ -444,6 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // ---- STEP: store the appended entry into the ring (every tile that
+    // staged its slot has been consumed)
+    if (has_new) {
+        if (threadIdx.x < 2 * NVR) {
+            uint4 *dst = static_cast<uint4 *>(threadIdx.x < NVR ? p.ring_k : p.ring_v);
+            dst[(((int64_t)b * p.n_kv_heads + kvh) * p.n_slots + new_slot) * NVR + threadIdx.x % NVR] =
+                s_new[threadIdx.x];
+        }
+        if (kvh == 0 && threadIdx.x == 0) p.tag_w[(int64_t)b * p.n_slots + new_slot] = (int32_t)qpos0;
+    }
+
     // ---- row sums across lanes and warps, normalise, write
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -503,12 +555,29 @@ cudaError_t launch_attn_mt(const CUtensorMap &k, const CUtensorMap &v, const Att
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(attn_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(attn_kernel<D, MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    return launch_pdl(attn_kernel<D, MT>, grid, dim3(kThreads), smem, stream, k, v, p);
+    return launch_pdl(attn_kernel<D, MT, false>, grid, dim3(kThreads), smem, stream, k, v, p);
+}
+
+template <int D, int MT>
+cudaError_t launch_step_mt(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, cudaStream_t stream) {
+    constexpr int smem = AttnSmem<D, MT>::TOTAL;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(attn_kernel<D, MT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
+    return launch_pdl(attn_kernel<D, MT, true>, grid, dim3(kThreads), smem, stream, k, v, p);
 }
 
 template <int D>
@@ -519,6 +588,46 @@ cudaError_t launch_attn(const CUtensorMap &k, const CUtensorMap &v, const AttnPa
         case 2: return launch_attn_mt<D, 2>(k, v, p, stream);
         case 3: return launch_attn_mt<D, 3>(k, v, p, stream);
         case 4: return launch_attn_mt<D, 4>(k, v, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D, int MT, bool STEP>
+int blocks_per_sm_mt() {
+    constexpr int smem = AttnSmem<D, MT>::TOTAL;
+    if (cudaFuncSetAttribute(attn_kernel<D, MT, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, MT, STEP>, kThreads, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D>
+int blocks_per_sm(int m_tiles, bool step) {
+    switch (m_tiles) {
+        case 1: return step ? blocks_per_sm_mt<D, 1, true>() : blocks_per_sm_mt<D, 1, false>();
+        case 2: return step ? blocks_per_sm_mt<D, 2, true>() : blocks_per_sm_mt<D, 2, false>();
+        case 3: return step ? blocks_per_sm_mt<D, 3, true>() : blocks_per_sm_mt<D, 3, false>();
+        case 4: return step ? blocks_per_sm_mt<D, 4, true>() : blocks_per_sm_mt<D, 4, false>();
+        default: return 0;
+    }
+}
+
+template <int D>
+cudaError_t launch_step(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
+                        cudaStream_t stream) {
+    switch (m_tiles) {
+        case 1: return launch_step_mt<D, 1>(k, v, p, stream);
+        case 2: return launch_step_mt<D, 2>(k, v, p, stream);
+        case 3: return launch_step_mt<D, 3>(k, v, p, stream);
+        case 4: return launch_step_mt<D, 4>(k, v, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -8,6 +8,11 @@
 // (one float4 each) x 16 part groups, so the loads of different parts are
 // independent and in flight together; the 16 group sums meet in shared
 // memory.  Every CTA of a row recomputes the row's lse (n_parts floats).
+//
+// After a fused draft step the merge also commits the append: the first CTA
+// of each sequence's rows advances n_seen[b] by one.  The attention grid has
+// completed by then (this kernel waits for it), so no CTA of it can have
+// read the new count.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -27,7 +32,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 __global__ void __launch_bounds__(kMergeThreads)
     lse_merge_kernel(const float *__restrict__ o_parts, const float *__restrict__ lse_parts, int n_parts,
-                     int head_dim, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out) {
+                     int head_dim, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out,
+                     int64_t *__restrict__ commit_n_seen, int rows_per_seq) {
     __shared__ float red[kMergeThreads / 32];
     __shared__ float4 acc_s[kPartGroups][kColThreads];
     pdl_wait();
@@ -35,6 +41,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int64_t r = blockIdx.x;
     const float *ls = lse_parts + r * n_parts;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (commit_n_seen && blockIdx.y == 0 && tid == 0 && r % rows_per_seq == 0) {
+        const int64_t b = r / rows_per_seq;
+        const int64_t seen = commit_n_seen[b];
+        if (seen >= 0) commit_n_seen[b] = seen + 1;  // a negative count was reported, nothing appended
+    }
 
     float mx = -CUDART_INF_F;
     for (int s = tid; s < n_parts; s += kMergeThreads) mx = fmaxf(mx, ls[s]);
@@ -97,11 +108,13 @@ __global__ void __launch_bounds__(kMergeThreads)
 }  // namespace
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows,
-                             int head_dim, void *out, float *lse_out, const int32_t *, cudaStream_t stream) {
+                             int head_dim, void *out, float *lse_out, int64_t *commit_n_seen, int rows_per_seq,
+                             cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     const dim3 grid((unsigned)rows, (unsigned)((head_dim + 4 * kColThreads - 1) / (4 * kColThreads)));
     return launch_pdl(lse_merge_kernel, grid, dim3(kMergeThreads), 0, stream, o_parts, lse_parts, n_parts,
-                      head_dim, static_cast<__nv_bfloat16 *>(out), lse_out);
+                      head_dim, static_cast<__nv_bfloat16 *>(out), lse_out, commit_n_seen,
+                      rows_per_seq > 0 ? rows_per_seq : 1);
 }
 
 }  // namespace wm

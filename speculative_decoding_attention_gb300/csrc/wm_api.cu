@@ -95,19 +95,45 @@ int key_tile(int op, int head_dim) { return use_tc_kernel(op, head_dim) ? kTcTil
 // K+V bytes per split when a batch may be ragged (see plan_splits).
 constexpr int64_t kRaggedSplitBytes = 8ll << 20;
 
+// Resident CTAs per SM of the kernel that serves `op` (the tcgen05 verify
+// kernel: one).  For the draft the smaller of the plain and the fused-step
+// instances, so that both split alike.  At least 1 (also without a device).
+int ctas_per_sm(int op, int head_dim, int rows) {
+    if (use_tc_kernel(op, head_dim)) return 1;
+    static std::mutex mu;
+    static int cache[kMaxDevices][3][4][2] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+    const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+    const int mt = std::min(4, std::max(1, (rows + 15) / 16));
+    const int oi = op == WM_OP_VERIFY ? 1 : 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int &n = cache[dev][di][mt - 1][oi];
+    if (!n) {
+        auto query = [&](bool step) {
+            return di == 0 ? attn_blocks_per_sm_d64(mt, step)
+                 : di == 1 ? attn_blocks_per_sm_d128(mt, step) : attn_blocks_per_sm_d256(mt, step);
+        };
+        const int plain = query(false);
+        n = std::max(1, oi ? plain : std::min(plain, query(true)));
+    }
+    return n;
+}
+
 // Key splits for `units` (sequence, KV head) pairs over up to max_keys keys,
-// never a split smaller than a tile.  By default: one wave of one CTA per SM.
+// never a split smaller than a tile.  By default: one wave of the kernel's
+// resident CTAs (per_sm per SM).
 // With several sequences the lengths may differ (only their maximum is known
 // on the host), so splits are also capped at about kRaggedSplitBytes of K+V:
 // short sequences then leave most of their splits empty (those CTAs exit at
 // once) and the block scheduler balances the rest.
-SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim) {
+SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim, int per_sm) {
     SplitPlan pl;
     const int64_t tiles = std::max<int64_t>(1, (max_keys + tile - 1) / tile);
     int64_t ns = requested;
     if (ns <= 0) {
         const int sms = sm_count();
-        ns = std::max<int64_t>(1, (sms > 0 ? sms : 1) / std::max(1, units));
+        ns = std::max<int64_t>(1, (int64_t)per_sm * (sms > 0 ? sms : 1) / std::max(1, units));
         if (batch > 1) {
             const int64_t keys_cap = std::max<int64_t>(tile, kRaggedSplitBytes / (4 * head_dim) / tile * tile);
             ns = std::max<int64_t>(ns, (max_keys + keys_cap - 1) / keys_cap);
@@ -191,16 +217,24 @@ int32_t wm_version(void) { return 100; }
 
 int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
                        int32_t head_dim, int64_t max_keys, int32_t n_split) {
-    if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY) || batch <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 ||
-        n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
+    if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY && op != WM_OP_DRAFT_STEP) || batch <= 0 || n_kv_heads <= 0 ||
+        n_q_heads <= 0 || n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
         return 0;
-    return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim).n_split;
+    if (op == WM_OP_DRAFT_STEP) {
+        if (n_q != 1) return 0;
+        op = WM_OP_DRAFT;  // the fused step splits exactly as the draft attention does
+    }
+    return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim,
+                       ctas_per_sm(op, head_dim, n_q * (n_q_heads / n_kv_heads)))
+        .n_split;
 }
 
 size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
                          int32_t head_dim, int64_t max_keys, int32_t n_split) {
     const int32_t ns = wm_plan_splits(op, batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split);
     if (ns <= 0) return (size_t)-1;
+    if (op == WM_OP_DRAFT_STEP)  // partials even when unsplit: the merge commits the append
+        return partial_bytes((int64_t)batch * n_q_heads, ns, head_dim);
     if (ns == 1) return 0;
     return partial_bytes((int64_t)batch * n_q * n_q_heads, ns, head_dim);
 }
@@ -267,7 +301,7 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
     if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 8) || (lse_out && !aligned(lse_out, 4)))
         return WM_ERR_INVALID_ARG;
     if (head_dim % 4) return WM_ERR_UNSUPPORTED;
-    return launch_status(launch_lse_merge(o_parts, lse_parts, n_parts, rows, head_dim, out, lse_out, nullptr,
+    return launch_status(launch_lse_merge(o_parts, lse_parts, n_parts, rows, head_dim, out, lse_out, nullptr, 0,
                                           static_cast<cudaStream_t>(stream)));
 }
 
@@ -277,7 +311,8 @@ static wm_status run_attention(int op, AttnParams &p, const CUtensorMap &mk, con
                                int64_t max_keys, int32_t n_split, void *out, float *lse, void *ws,
                                size_t ws_bytes, cudaStream_t st) {
     const SplitPlan pl =
-        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim), p.head_dim);
+        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim), p.head_dim,
+                    ctas_per_sm(op, p.head_dim, p.rows));
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
     p.n_split = pl.n_split;
     p.keys_per_split = pl.keys_per_split;
@@ -295,7 +330,7 @@ static wm_status run_attention(int op, AttnParams &p, const CUtensorMap &mk, con
     cudaError_t e = launch_attn_any(op, mk, mv, p, st);
     if (e != cudaSuccess) return WM_ERR_CUDA;
     if (pl.n_split > 1) {
-        e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, st);
+        e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, 0, st);
         if (e != cudaSuccess) return WM_ERR_CUDA;
     }
     return WM_OK;
@@ -339,6 +374,75 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
     p.err = err;
     return run_attention(WM_OP_DRAFT, p, mk, mv, n_slots, n_split, out, lse, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
+}
+
+wm_status wm_draft_step(const wm_ring *ring, const void *k_new, const void *v_new, const void *q,
+                        int32_t n_q_heads, float scale, int32_t n_split, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    if (!ring_ok(ring) || !k_new || !v_new || !q || !out || n_q_heads <= 0 || n_split < 0 ||
+        !std::isfinite(scale))
+        return WM_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)))
+        return WM_ERR_INVALID_ARG;
+    if (n_q_heads % ring->n_kv_heads) return WM_ERR_INVALID_ARG;
+    const int group = n_q_heads / ring->n_kv_heads;
+    if (group > kMaxRows) return WM_ERR_UNSUPPORTED;
+    const int n_slots = ring->sink + ring->window;
+    const SplitPlan pl = plan_splits(ring->batch * ring->n_kv_heads, ring->batch, n_slots, n_split, kKeyTile,
+                                     ring->head_dim, ctas_per_sm(WM_OP_DRAFT, ring->head_dim, group));
+    const int64_t rows_total = (int64_t)ring->batch * n_q_heads;
+    const size_t need = partial_bytes(rows_total, pl.n_split, ring->head_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return WM_ERR_WORKSPACE;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile) ||
+        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile))
+        return WM_ERR_CUDA;
+    AttnParams p;
+    std::memset(&p, 0, sizeof p);
+    p.source = KEYS_RING;
+    p.batch = ring->batch;
+    p.n_kv_heads = ring->n_kv_heads;
+    p.head_dim = ring->head_dim;
+    p.pos_tag = ring->pos_tag;
+    p.n_seen = ring->n_seen;
+    p.n_slots = n_slots;
+    p.sink = ring->sink;
+    p.window = ring->window;
+    p.capacity = n_slots;
+    p.box_rows = kKeyTile;
+    p.q = q;
+    p.n_q = 1;
+    p.n_q_heads = n_q_heads;
+    p.group = group;
+    p.rows = group;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.n_split = pl.n_split;
+    p.keys_per_split = pl.keys_per_split;
+    p.out = out;
+    p.lse = lse;
+    const size_t o_bytes = (size_t)rows_total * pl.n_split * ring->head_dim * sizeof(float);
+    p.o_part = static_cast<float *>(workspace);
+    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((o_bytes + 255) & ~(size_t)255));
+    p.err = err;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.ring_k = ring->k;
+    p.ring_v = ring->v;
+    p.tag_w = ring->pos_tag;
+    const int m_tiles = (group + 15) / 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (ring->head_dim) {
+        case 64: e = launch_step_d64(mk, mv, p, m_tiles, st); break;
+        case 128: e = launch_step_d128(mk, mv, p, m_tiles, st); break;
+        default: e = launch_step_d256(mk, mv, p, m_tiles, st); break;
+    }
+    if (e != cudaSuccess) return WM_ERR_CUDA;
+    return launch_status(launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, ring->head_dim, out, lse,
+                                          ring->n_seen, n_q_heads, st));
 }
 
 wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_q_heads, float scale,

@@ -16,8 +16,11 @@ enum KeySource : int32_t {
 
 // Keys handled per pipeline stage by the attention kernel (all head dims).
 constexpr int kKeyTile = 64;
-// Shared-memory bytes given to KV staging (stages = this / stage bytes).
-constexpr int kStagingBytes = 128 * 1024;
+// Shared-memory bytes the mma.sync attention kernel gives to K/V staging
+// (stages = this / stage bytes): 4 stages of 64 keys at head_dim 64 and 128 --
+// small enough for two CTAs per SM, whose independent tile loops overlap --
+// and the two stages head_dim 256 needs at one CTA per SM.
+constexpr int staging_bytes(int head_dim) { return head_dim == 256 ? 128 * 1024 : 64 * 1024; }
 // Consumer warps + one producer warp.
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -59,6 +62,12 @@ struct AttnParams {
     float *o_part;        // [B*n_q*Hq][n_split][D] fp32, NULL when unsplit
     float *lse_part;      // [B*n_q*Hq][n_split]
     int32_t *err;         // device error word
+    // fused draft step (ring append + draft attention in one launch)
+    const void *k_new;    // [B][Hkv][D] bf16: the entries appended at p = n_seen[b]
+    const void *v_new;
+    void *ring_k;         // the ring's K and V, written at slot(p)
+    void *ring_v;
+    int32_t *tag_w;       // writable pos_tag of the ring
 };
 
 // Launch the attention kernel for head dim D (defined in attn_d<D>.cu).
@@ -68,6 +77,21 @@ cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const A
                              int m_tiles, cudaStream_t stream);
 cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
                              int m_tiles, cudaStream_t stream);
+
+// Resident CTAs per SM of the mma.sync attention kernel for head dim D with
+// m_tiles row tiles (step: the fused draft-step instance); 0 if unknown.
+int attn_blocks_per_sm_d64(int m_tiles, bool step);
+int attn_blocks_per_sm_d128(int m_tiles, bool step);
+int attn_blocks_per_sm_d256(int m_tiles, bool step);
+
+// Fused draft step (ring append + draft attention) for head dim D; always
+// writes split partials (o_part / lse_part) for the merge kernel.
+cudaError_t launch_step_d64(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
+                            cudaStream_t stream);
+cudaError_t launch_step_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
+                             cudaStream_t stream);
+cudaError_t launch_step_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
+                             cudaStream_t stream);
 
 // Tensor-core (tcgen05) attention kernel for head dims 128 and 256 (attn_tc_d<D>.cu);
 // n_rows16 is the row count per KV head rounded up to 16, 128-key tiles.
@@ -101,8 +125,11 @@ cudaError_t launch_ring_fill(void *rk, void *rv, int32_t *tag, int64_t *n_seen, 
 cudaError_t launch_ring_rollback(int32_t *tag, int64_t *n_seen, int batch, int n_slots,
                                  const int64_t *new_len, int32_t *err, cudaStream_t stream);
 
+// Merge of split partials.  With commit_n_seen != NULL (the fused draft step)
+// it also advances n_seen[b] by one for every sequence b whose value is >= 0;
+// rows_per_seq rows of the output belong to each sequence.
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n_parts,
                              int64_t rows, int head_dim, void *out, float *lse_out,
-                             const int32_t *row_map, cudaStream_t stream);
+                             int64_t *commit_n_seen, int rows_per_seq, cudaStream_t stream);
 
 }  // namespace wm

@@ -17,12 +17,12 @@ import torch
 from . import build as _build
 
 WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, WM_ERR_DEVICE_DATA = range(6)
-WM_OP_DRAFT, WM_OP_VERIFY = 0, 1
+WM_OP_DRAFT, WM_OP_VERIFY, WM_OP_DRAFT_STEP = 0, 1, 2
 DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout", 4: "internal check"}
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
-            "wm_status_string", "wm_version", "wm_draft_attn_static")
+            "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step")
 STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
 
 _lib = None
@@ -69,6 +69,7 @@ def load() -> ctypes.CDLL:
         lib.wm_draft_attn.argtypes = [P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_verify_attn.argtypes = [P, P, I32, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_draft_attn_static.argtypes = [P, P, I32, F, I32, P, P, P]
+        lib.wm_draft_step.argtypes = [P, P, P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_lse_merge.argtypes = [P, P, I32, I64, I32, P, P, P]
         lib.wm_plan_splits.argtypes = [I32, I32, I32, I32, I32, I32, I64, I32]
         lib.wm_plan_splits.restype = I32
@@ -264,6 +265,35 @@ def draft_attn(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=
     _check(load().wm_draft_attn(ctypes.byref(r), _dev(q, torch.bfloat16, "q"), Hq, float(scale), n_split,
                                 _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"), ws,
                                 ws_bytes, _stream(stream)), "wm_draft_attn")
+    return out, lse
+
+
+def step_workspace(ring: Ring, n_q_heads: int, n_split: int = 0, device=None) -> torch.Tensor:
+    """A workspace for draft_step on this ring (split partials; never empty)."""
+    need = workspace_size(WM_OP_DRAFT_STEP, ring.batch, ring.n_kv_heads, n_q_heads, 1, ring.head_dim,
+                          ring.sink + ring.window, n_split)
+    return torch.empty(need, dtype=torch.uint8, device=device if device is not None else ring.k.device)
+
+
+def draft_step(ring: Ring, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, scale: float,
+               workspace: torch.Tensor, n_split: int = 0, out=None, lse=None, stream=None):
+    """Fused ring append + draft attention: append (k_new, v_new) [B, Hkv, D]
+    at p = n_seen[b] and attend q [B, Hq, D] from position p over the sinks and
+    the window, in one attention launch (plus the split merge, which commits
+    n_seen).  ``workspace`` comes from step_workspace().  Returns (out bf16,
+    lse fp32), bit-identical to ring_append followed by draft_attn."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    r = ring.c()
+    _check(load().wm_draft_step(ctypes.byref(r), _dev(k_new, torch.bfloat16, "k_new"),
+                                _dev(v_new, torch.bfloat16, "v_new"), _dev(q, torch.bfloat16, "q"), Hq,
+                                float(scale), n_split, _dev(out, torch.bfloat16, "out"),
+                                _dev(lse, torch.float32, "lse"), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "wm_draft_step")
     return out, lse
 
 

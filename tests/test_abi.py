@@ -109,6 +109,39 @@ def test_bad_verify_shapes(lib, over, n_q, hq, status):
                               None) == status
 
 
+def test_draft_step_rejects_bad_arguments(lib):
+    r = _ring()
+    P = ctypes.c_void_p
+    q, out, ws = P(1 << 24), P(1 << 25), P(1 << 26)
+
+    def call(k_new=P(1 << 23), v_new=P(3 << 22), hq=8, scale=1.0, ws_ptr=ws, ws_bytes=1 << 20, ring=r):
+        # an explicit split count: the plan needs no device query
+        return lib.wm_draft_step(ctypes.byref(ring), k_new, v_new, q, hq, scale, 4, out, None, ws_ptr, ws_bytes,
+                                 None)
+
+    assert lib.wm_draft_step(None, P(16), P(16), q, 8, 1.0, 0, out, None, ws, 1 << 20, None) == \
+        wm.WM_ERR_INVALID_ARG
+    assert call(k_new=None) == wm.WM_ERR_INVALID_ARG
+    assert call(v_new=P((1 << 23) + 8)) == wm.WM_ERR_INVALID_ARG      # misaligned
+    assert call(hq=7) == wm.WM_ERR_INVALID_ARG                         # 7 heads over 2 KV heads
+    assert call(scale=float("inf")) == wm.WM_ERR_INVALID_ARG
+    assert call(ring=_ring(head_dim=96)) == wm.WM_ERR_INVALID_ARG
+    assert call(ws_ptr=None) == wm.WM_ERR_WORKSPACE
+    assert call(ws_ptr=P((1 << 26) + 16)) == wm.WM_ERR_WORKSPACE      # not 256-byte aligned
+    assert call(ws_bytes=8) == wm.WM_ERR_WORKSPACE
+
+
+def test_draft_step_workspace(lib):
+    # split partials (o then lse) even when unsplit: the merge commits n_seen
+    for ns in (1, 4, 5):  # split counts the 65 tiles of 4100 slots divide into exactly
+        rows, D = 16, 128
+        o = rows * ns * D * 4
+        assert wm.workspace_size(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 1, D, 4100, ns) == \
+            ((o + 255) // 256) * 256 + rows * ns * 4
+    assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 1, 256, 4100, 1000) == 65  # one tile per split at most
+    assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 2, 256, 4100, 4) == 0      # one query position only
+
+
 def test_workspace_size_with_explicit_splits(lib):
     # Explicit split counts need no device query.
     assert wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, 1) == 0

@@ -2,7 +2,8 @@
 
 Each workload's step state is built exactly as the bench builds it (ring fill,
 and for the NoPE workload 20,000 single appends that wrap the window), then:
-every draft row of every draft step is compared with the oracle; the verify is
+every draft row of every draft step (fused and unfused) is compared with the
+oracle; the verify is
 compared on a sample of rows the oracle evaluates one by one (first, last and
 evenly spaced rows of the [batch, T, Hq] space); the ring's tags are compared
 with the StreamingLLM cache model.
@@ -39,14 +40,22 @@ def test_full_size_step(name):
         t = tags[b]
         assert sorted(int(x) for x in t[t >= 0]) == held_after(w.sink, w.window, n)
 
-    st.run()
-    torch.cuda.synchronize()
-    assert wm.get_device_error() == 0
     hist = oracle_kv(inp.k, inp.v, inp.block_table)
-    for j in range(depth):
-        pos = [n + j for n in inp.seq_lens_host]
-        ref, ref_lse = oracle.draft(hist, inp.q_draft[j].cpu(), pos, w.sink, w.window, w.scale)
-        assert_close(f"{name} draft step {j}", st.d_out[j], st.d_lse[j], ref, ref_lse)
+    refs = [oracle.draft(hist, inp.q_draft[j].cpu(), [n + j for n in inp.seq_lens_host], w.sink, w.window,
+                         w.scale) for j in range(depth)]
+    # the unfused draft (append, attention, merge) first, then the fused step the bench times, each
+    # from the ring as built (a rollback does not restore the window entries the appends overwrote)
+    saved = [t.clone() for t in (st.ring.k, st.ring.v, st.ring.pos_tag, st.ring.n_seen)]
+    for fused in (False, True):
+        for t, c in zip((st.ring.k, st.ring.v, st.ring.pos_tag, st.ring.n_seen), saved):
+            t.copy_(c)
+        st.run(fused=fused)
+        torch.cuda.synchronize()
+        assert wm.get_device_error() == 0
+        for j, (ref, ref_lse) in enumerate(refs):
+            assert_close(f"{name} draft step {j} ({'fused' if fused else 'unfused'})", st.d_out[j], st.d_lse[j],
+                         ref, ref_lse)
+        assert st.ring.n_seen.tolist() == list(inp.seq_lens_host)  # rolled back
 
     T, Hq, D = st.T, w.n_q_heads, w.head_dim
     total = w.batch * T * Hq
