@@ -72,9 +72,11 @@ def _load(plant: int = 0) -> ctypes.CDLL:
         P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.wmo_verify.argtypes = [ctypes.POINTER(_KV), I32, I32, P, P, D, P, I64, P, P]
         lib.wmo_draft.argtypes = [ctypes.POINTER(_KV), I32, P, P, I64, I64, D, P, I64, P, P]
+        lib.wmo_draft_mem.argtypes = [ctypes.POINTER(_KV), ctypes.POINTER(_KV), P, I32, P, P, I64, I64, D, P,
+                                      I64, P, P]
         lib.wmo_attend_subset.argtypes = [P, P, P, P, I64, I32, D, P, P]
         lib.wmo_lse_merge.argtypes = [P, P, I32, I64, I32, P, P]
-        for f in (lib.wmo_verify, lib.wmo_draft, lib.wmo_attend_subset, lib.wmo_lse_merge):
+        for f in (lib.wmo_verify, lib.wmo_draft, lib.wmo_draft_mem, lib.wmo_attend_subset, lib.wmo_lse_merge):
             f.restype = ctypes.c_int
         lib.wmo_num_threads.restype = ctypes.c_int
         _libs[plant] = lib
@@ -198,6 +200,30 @@ def draft(hist: KV, q, pos, sink: int, window: int, scale: float, rows=None, pla
                                 float(scale), _ptr(r), n, _ptr(out), _ptr(lse))
     if rc:
         raise ValueError(f"oracle draft failed ({rc})")
+    return out, lse
+
+
+def draft_mem(hist: KV, mem: KV, mem_count, q, pos, sink: int, window: int, scale: float, rows=None,
+              plant: int = 0):
+    """Sink + window attention plus every materialized memory slot
+    (memory-augmented sliding-window drafting).
+
+    mem: contiguous store [batch, Hkv, capacity, D] of memory-slot K/V;
+    mem_count: [batch] slots materialized so far.  Otherwise as draft().
+    """
+    qb = _bits(q)
+    B, Hq, D = qb.shape
+    p = _i64(pos)
+    mc = _i64(mem_count)
+    _check_batch(hist, B, p.size, D)
+    _check_batch(mem, B, mc.size, D)
+    r, n = _rows(rows, B * Hq)
+    out = np.zeros((n, D), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load(plant).wmo_draft_mem(ctypes.byref(hist.c), ctypes.byref(mem.c), _ptr(mc), Hq, _ptr(qb), _ptr(p),
+                                    int(sink), int(window), float(scale), _ptr(r), n, _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle draft_mem failed ({rc})")
     return out, lse
 
 

@@ -26,6 +26,11 @@
  * no running rescale.  Rows are independent; OpenMP only spreads whole rows
  * over the host cores and changes no arithmetic.
  *
+ *   - Memory-augmented draft ("Memory-Augmented Sliding-Window Drafting", 4.1
+ *     and Appendix C).  The draft's working memory is the sinks, the exact
+ *     local window and the compressed memory slots materialized so far; a
+ *     raw-token query attends to all three, M(p) plus slots 0..count-1.
+ *
  * The log-sum-exp merge of partial results is the textbook identity
  *     lse = M + ln sum_s exp(lse_s - M),  o = sum_s exp(lse_s - lse) o_s.
  *
@@ -267,6 +272,105 @@ int wmo_draft(const wmo_kv *hist, int n_q_heads, const uint16_t *q, const int64_
         keyset ks = { KEYS_SINK_WINDOW, pos[b], sink, window };
         if (attend_row(hist, b, kv_head_of(h, n_q_heads, hist->n_kv_heads), q + r * D, scale, &ks,
                        out + s * D, lse + s))
+            err = -2;
+    }
+    return err;
+}
+
+/* Memory-augmented sliding-window draft ("Memory-Augmented Sliding-Window
+ * Drafting", 4.1 and Appendix C): the working memory of the draft is the
+ * union of the attention sinks, the exact local window and the compressed
+ * memory slots materialized so far, and an ordinary raw-token query sees
+ * exactly those.  So for a query at position p of sequence b the key set is
+ * M(p) over the draft history (as in wmo_draft) plus memory slots
+ * 0..mem_count[b]-1 of `mem`, under one softmax.  The slots' K/V come from
+ * the draft's adaptor; here they are inputs.  mem is a contiguous store
+ * [batch][n_kv_heads][capacity][head_dim] (its n_cap is the capacity). */
+static int attend_row_mem(const wmo_kv *hist, const wmo_kv *mem, int64_t n_mem, int b, int h,
+                          const uint16_t *q, double scale, const keyset *ks, double *out, double *lse)
+{
+    const int D = hist->head_dim;
+    const int64_t n_pos = ks->pos + 1 > 0 ? ks->pos + 1 : 0;
+#if WMO_PLANT == 9
+    n_mem = n_mem > 0 ? n_mem - 1 : 0; /* planted: the newest memory slot dropped */
+#endif
+    double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(n_pos + n_mem > 0 ? n_pos + n_mem : 1));
+    int rc = 0;
+    for (int d = 0; d < D; ++d) qd[d] = bf16_to_double(q[d]);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+
+    /* pass 1: logits of the window members (index j) and the slots (n_pos + s) */
+    double m = -INFINITY;
+    int64_t n_members = 0;
+    for (int64_t i = 0; i < n_pos + n_mem; ++i) {
+        const uint16_t *kr;
+        if (i < n_pos) {
+            if (!in_keyset(ks, i)) continue;
+            kr = kv_row(hist, hist->k, b, h, i);
+        } else {
+            kr = kv_row(mem, mem->k, b, h, i - n_pos);
+        }
+        if (!kr) { rc = -1; goto done; }
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qd[d] * bf16_to_double(kr[d]);
+        logit[i] = scale * dot;
+        if (logit[i] > m) m = logit[i];
+        ++n_members;
+    }
+    if (n_members == 0) { *lse = -INFINITY; goto done; }
+
+    /* pass 2: normaliser and weighted sum of the values */
+    double z = 0.0;
+    for (int64_t i = 0; i < n_pos + n_mem; ++i) {
+        const uint16_t *vr;
+        if (i < n_pos) {
+            if (!in_keyset(ks, i)) continue;
+            vr = kv_row(hist, hist->v, b, h, i);
+        } else {
+            vr = kv_row(mem, mem->v, b, h, i - n_pos);
+        }
+        if (!vr) { rc = -1; goto done; }
+        double w = exp(logit[i] - m);
+        z += w;
+        for (int d = 0; d < D; ++d) out[d] += w * bf16_to_double(vr[d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= z;
+    *lse = m + log(z);
+done:
+    free(qd);
+    free(logit);
+    return rc;
+}
+
+/* Draft attention over sinks + window + memory slots.  As wmo_draft, plus
+ * mem (contiguous, same batch / heads / head_dim as hist) and mem_count
+ * [batch]: slots materialized so far (0..capacity).  Returns -1 on bad
+ * arguments, -2 if a key has no storage. */
+int wmo_draft_mem(const wmo_kv *hist, const wmo_kv *mem, const int64_t *mem_count, int n_q_heads,
+                  const uint16_t *q, const int64_t *pos, int64_t sink, int64_t window, double scale,
+                  const int64_t *rows, int64_t n_rows, double *out, double *lse)
+{
+    if (check_kv(hist) || check_kv(mem) || mem->block_table || !mem_count || !q || !pos || !out || !lse ||
+        n_q_heads <= 0)
+        return -1;
+    if (n_q_heads % hist->n_kv_heads || sink < 0 || window < 1) return -1;
+    if (mem->batch != hist->batch || mem->n_kv_heads != hist->n_kv_heads || mem->head_dim != hist->head_dim)
+        return -1;
+    const int64_t total = (int64_t)hist->batch * n_q_heads;
+    const int64_t n = rows ? n_rows : total;
+    const int D = hist->head_dim;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t s = 0; s < n; ++s) {
+        int64_t r = rows ? rows[s] : s;
+        if (r < 0 || r >= total) { err = -1; continue; }
+        int b = (int)(r / n_q_heads);
+        int h = (int)(r % n_q_heads);
+        if (mem_count[b] < 0 || mem_count[b] > mem->n_cap) { err = -1; continue; }
+        keyset ks = { KEYS_SINK_WINDOW, pos[b], sink, window };
+        if (attend_row_mem(hist, mem, mem_count[b], b, kv_head_of(h, n_q_heads, hist->n_kv_heads), q + r * D,
+                           scale, &ks, out + s * D, lse + s))
             err = -2;
     }
     return err;

@@ -9,7 +9,9 @@ deliberate mistake at a time and checks that some pin fails for each.
 
 Pages: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at Million-Token
 Context" (Abstract) -- draft attention over a sliding window plus attention
-sinks, full-attention verification intact.
+sinks, full-attention verification intact; "Memory-Augmented Sliding-Window
+Drafting" (4.1, Appendix C) -- the draft's working memory adds compressed
+memory slots to the sinks and the window.
 """
 import math
 
@@ -318,6 +320,68 @@ def test_key_order_does_not_matter():
     assert close(a[0], b[0]) and a[1] == pytest.approx(b[1], rel=1e-13)
 
 
+# ------------------------------------------------------------ memory slots
+
+def _draft_mem_case(plant=0, seed=21):
+    """Memory-augmented draft: for several (S, W, p, slot count) the oracle
+    equals dense fp64 softmax attention (torch) over the keys a sink-list +
+    deque cache holds after positions 0..p, concatenated with the first
+    `count` memory slots -- per sequence, with two query heads per KV head."""
+    g = torch.Generator().manual_seed(seed)
+    B, Hkv, G, N, cap, D = 2, 2, 2, 60, 9, 16
+    k, v = rand_bf16((B, Hkv, N, D), g), rand_bf16((B, Hkv, N, D), g)
+    mk, mv = rand_bf16((B, Hkv, cap, D), g), rand_bf16((B, Hkv, cap, D), g)
+    hist, mem = oracle.KV(k, v), oracle.KV(mk, mv)
+    for S, W, pos, counts in [(4, 8, [59, 30], [9, 3]), (0, 5, [10, 59], [1, 0]), (2, 60, [59, 0], [4, 9]),
+                              (1, 1, [0, 1], [9, 9])]:
+        q = rand_bf16((B, Hkv * G, D), g)
+        out, lse = oracle.draft_mem(hist, mem, counts, q, pos, S, W, 0.4, plant=plant)
+        for b in range(B):
+            cache = StreamingCache(S, W)
+            for p in range(pos[b] + 1):
+                cache.append(p)
+            held = torch.tensor(cache.held(), dtype=torch.long)
+            for h in range(Hkv * G):
+                kvh = h // G
+                keys = torch.cat([f64(k[b, kvh])[held], f64(mk[b, kvh, :counts[b]])])
+                vals = torch.cat([f64(v[b, kvh])[held], f64(mv[b, kvh, :counts[b]])])
+                logit = (keys @ f64(q[b, h])) * 0.4
+                ref = torch.softmax(logit, 0) @ vals
+                r = b * Hkv * G + h
+                if not (close(out[r], ref.numpy()) and abs(lse[r] - float(torch.logsumexp(logit, 0))) < 1e-12):
+                    return False
+    return True
+
+
+def test_draft_with_memory_slots_matches_dense_softmax_over_the_union():
+    assert _draft_mem_case()
+
+
+def test_no_memory_slot_reduces_to_the_windowed_draft():
+    g = torch.Generator().manual_seed(22)
+    B, Hkv, N, D = 2, 2, 80, 32
+    k, v = rand_bf16((B, Hkv, N, D), g), rand_bf16((B, Hkv, N, D), g)
+    mk, mv = rand_bf16((B, Hkv, 5, D), g), rand_bf16((B, Hkv, 5, D), g)
+    q = rand_bf16((B, 4, D), g)
+    a = oracle.draft(oracle.KV(k, v), q, [79, 40], 4, 16, 0.3)
+    m = oracle.draft_mem(oracle.KV(k, v), oracle.KV(mk, mv), [0, 0], q, [79, 40], 4, 16, 0.3)
+    assert np.array_equal(a[0], m[0]) and np.array_equal(a[1], m[1])
+
+
+def test_memory_slot_equal_to_a_window_key_counts_twice():
+    # A slot holding a copy of the query's own key and value: exactly the
+    # two-key closed form when the window holds only that key.
+    g = torch.Generator().manual_seed(23)
+    D = 16
+    k, v = rand_bf16((1, 1, 3, D), g), rand_bf16((1, 1, 3, D), g)
+    mk, mv = k[:, :, 2:3].clone(), v[:, :, 2:3].clone()
+    q = rand_bf16((1, 1, D), g)
+    out, lse = oracle.draft_mem(oracle.KV(k, v), oracle.KV(mk, mv), [1], q, [2], 0, 1, 0.5)
+    l2 = 0.5 * float(f64(k[0, 0, 2]) @ f64(q[0, 0]))
+    assert close(out[0], f64(v[0, 0, 2]).numpy())
+    assert lse[0] == pytest.approx(l2 + math.log(2.0), rel=1e-13, abs=1e-13)
+
+
 # ------------------------------------------------------------ planted mistakes
 
 PLANTS = {
@@ -329,6 +393,7 @@ PLANTS = {
     6: "verify query drops its own key",
     7: "log-sum-exp loses its max term",
     8: "block table row of sequence 0 used for every sequence",
+    9: "newest memory slot dropped",
 }
 
 
@@ -342,9 +407,10 @@ def _passes(pin, plant):
 @pytest.mark.parametrize("plant", sorted(PLANTS))
 def test_planted_mistakes_are_caught(plant):
     caught = (not _passes(_verify_case, plant) or not _passes(_paged_case, plant)
-              or not _passes(lambda plant: _draft_bruteforce(plant=plant, n_tok=12), plant))
+              or not _passes(lambda plant: _draft_bruteforce(plant=plant, n_tok=12), plant)
+              or not _passes(_draft_mem_case, plant))
     assert caught, f"no pin caught the planted mistake: {PLANTS[plant]}"
 
 
 def test_unplanted_oracle_passes_the_planted_suite():
-    assert _verify_case() and _paged_case() and _draft_bruteforce(n_tok=12)
+    assert _verify_case() and _paged_case() and _draft_bruteforce(n_tok=12) and _draft_mem_case()
