@@ -327,6 +327,7 @@ def gpu_arm(args, rank, world, local):
     out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
     native_ms = native_draft_chain(st, flush, args)
     unfused_ms = unfused_draft_chain(st, flush, args)
+    masw = masw_draft_chain(st, flush, args)
 
     us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
     us_verify = 1e3 * sum(verify_ms) / len(verify_ms)
@@ -385,6 +386,7 @@ def gpu_arm(args, rank, world, local):
             "draft_l2": "L2 flushed before each step; draft steps 2..d re-read the ring (S+W slots) "
                         "mostly from L2, as a decode loop does",
             "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
+            "masw_draft": masw,
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
             "outputs_finite": out_ok,
             "steps_per_s_all_ranks": round(world * 1e6 / us_step, 1),
@@ -427,6 +429,59 @@ def unfused_draft_chain(st: Step, flush, args):
         if i >= max(3, args.warmup):
             ms.append(ev[0].elapsed_time(ev[1]))
     return sum(ms) / len(ms)
+
+
+MASW_SLOT_INTERVAL = 256  # one memory slot per 256 tokens of history
+
+
+def masw_draft_chain(st: Step, flush, args):
+    """The draft chain with memory slots (memory-augmented sliding window): the
+    fused step over sinks + window + one materialized slot per
+    MASW_SLOT_INTERVAL tokens of each sequence's history (synthetic slot K/V),
+    captured with in-graph events.  None without in-graph events."""
+    wm, w, inp = st.wm, st.w, st.inp
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    counts = [n // MASW_SLOT_INTERVAL for n in inp.seq_lens_host]
+    cap = max(1, max(counts))
+    gen = torch.Generator(device=st.dev).manual_seed(4242)
+    mem = wm.Mem.create(B, Hkv, D, cap, st.dev)
+    mem.k.copy_(torch.randn(mem.k.shape, generator=gen, device=st.dev).to(torch.bfloat16))
+    mem.v.copy_(torch.randn(mem.v.shape, generator=gen, device=st.dev).to(torch.bfloat16))
+    mem.count.copy_(torch.tensor(counts, dtype=torch.int64, device=st.dev))
+    ws = wm.step_workspace(st.ring, Hq, mem=mem)
+
+    def chain(ev=None):
+        if ev:
+            ev[0].record()
+        for j in range(st.d):
+            wm.draft_step(st.ring, inp.k_new[j], inp.v_new[j], inp.q_draft[j], w.scale, ws, out=st.d_out[j],
+                          lse=st.d_lse[j], mem=mem)
+        if ev:
+            ev[1].record()
+        wm.ring_rollback(st.ring, st.base_len)
+
+    chain()
+    torch.cuda.synchronize()
+    try:
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    except TypeError:
+        return None
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=st.dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        chain(ev)
+    ms = []
+    for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= max(3, args.warmup):
+            ms.append(ev[0].elapsed_time(ev[1]))
+    us = 1e3 * sum(ms) / len(ms) / st.d
+    kv_bytes = 2 * Hkv * D * 2 * sum(w.slots + c for c in counts)
+    return {"slot_interval": MASW_SLOT_INTERVAL, "slots": counts, "us_per_step": round(us, 2),
+            "kv_bytes_per_step": kv_bytes, "gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1)}
 
 
 def native_draft_chain(st: Step, flush, args) -> float:

@@ -91,6 +91,27 @@ typedef struct wm_ring {
 } wm_ring;
 
 /*
+ * Compressed memory slots of a memory-augmented sliding-window draft
+ * ("Memory-Augmented Sliding-Window Drafting", 4.1-4.3): at every r-token
+ * boundary the draft's adaptor materializes one memory slot (its K/V come
+ * from the caller; the adaptor is not part of this library) that stays after
+ * the raw tokens leave the window.  A draft query attends to the sinks, the
+ * window AND every slot materialized so far (wm_draft_attn_mem, wm_draft_step).
+ *   k, v     [batch][n_kv_heads][capacity][head_dim] bf16
+ *   count    [batch] int64: slots materialized so far, slot i at index i.
+ *            Initialise to 0.
+ */
+typedef struct wm_mem {
+    void *k;
+    void *v;
+    int64_t *count;
+    int64_t capacity; /* slots per (sequence, KV head), >= 1 */
+    int32_t batch;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+} wm_mem;
+
+/*
  * A full-context KV cache (the target's), contiguous or paged.
  *   contiguous (block_table == NULL):
  *       k, v  [batch][n_kv_heads][n_cap][head_dim] bf16
@@ -160,6 +181,34 @@ wm_status wm_ring_rollback(const wm_ring *ring, const int64_t *new_len, void *st
 wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale,
                         int32_t n_split, void *out, float *lse, void *workspace,
                         size_t workspace_bytes, void *stream);
+
+/*
+ * Memory-augmented draft attention ("Memory-Augmented Sliding-Window
+ * Drafting", 4.1 and Appendix C: a raw-token query sees the sink tokens, the
+ * available memory slots and a bounded local window).  As wm_draft_attn, and
+ * in the same softmax the query also attends to memory slots
+ * 0 .. mem->count[b]-1.  mem must match the ring's batch, n_kv_heads and
+ * head_dim.  A count outside 0..capacity records WM_DEVERR_BAD_LENGTH and is
+ * clamped.  Workspace: wm_workspace_size(WM_OP_DRAFT_MEM, ...) with
+ * max_keys = 64 * ceil((sink + window) / 64) + capacity.
+ */
+wm_status wm_draft_attn_mem(const wm_ring *ring, const wm_mem *mem, const void *q, int32_t n_q_heads,
+                            float scale, int32_t n_split, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * Materialize one memory slot per sequence: slot count[b] <- k_new[b], v_new[b]
+ * (all KV heads), then count[b] += 1.  k_new, v_new [batch][n_kv_heads][head_dim].
+ * A full store (count[b] == capacity) or a negative count records
+ * WM_DEVERR_BAD_LENGTH and leaves that sequence unchanged.
+ */
+wm_status wm_mem_append(const wm_mem *mem, const void *k_new, const void *v_new, void *stream);
+
+/*
+ * Rollback of memory slots materialized after the accepted prefix (4.3):
+ * count[b] = min(count[b], new_count[b]), new_count a device int64 [batch].
+ */
+wm_status wm_mem_rollback(const wm_mem *mem, const int64_t *new_count, void *stream);
 
 /*
  * Full-context verification attention (Abstract: full-attention verification
@@ -236,23 +285,28 @@ wm_status wm_draft_attn_static(const wm_ring *ring, const void *q, int32_t n_q_h
  *     and n_seen[b] = p + 1 -- the state wm_ring_append leaves.
  *   k_new, v_new  [batch][n_kv_heads][head_dim] bf16
  *   q, out        [batch][n_q_heads][head_dim] bf16;  lse [batch][n_q_heads] fp32 or NULL
+ *   mem           NULL, or memory slots the query also attends to (as
+ *                 wm_draft_attn_mem).
  *   n_split       as for wm_draft_attn (same plan).
  *   workspace     at least wm_workspace_size(WM_OP_DRAFT_STEP, batch, n_kv_heads,
- *                 n_q_heads, 1, head_dim, sink + window, n_split) bytes (never 0:
- *                 the split partials always pass through the merge, which
- *                 commits n_seen), 256-byte aligned; no initial contents needed.
- * out, lse and the ring are bit-identical to wm_ring_append + wm_draft_attn
- * with the same n_split.  A negative n_seen[b] records WM_DEVERR_BAD_LENGTH,
- * appends nothing for b and gives its rows out = 0, lse = -inf.
+ *                 n_q_heads, 1, head_dim, sink + window, n_split) bytes (with mem:
+ *                 WM_OP_DRAFT_MEM and its max_keys) -- never 0: the split
+ *                 partials always pass through the merge, which commits
+ *                 n_seen -- 256-byte aligned; no initial contents needed.
+ * out, lse and the ring are bit-identical to wm_ring_append followed by
+ * wm_draft_attn (wm_draft_attn_mem) with the same n_split.  A negative
+ * n_seen[b] records WM_DEVERR_BAD_LENGTH, appends nothing for b and gives its
+ * rows out = 0, lse = -inf.
  */
-wm_status wm_draft_step(const wm_ring *ring, const void *k_new, const void *v_new, const void *q,
-                        int32_t n_q_heads, float scale, int32_t n_split, void *out, float *lse,
-                        void *workspace, size_t workspace_bytes, void *stream);
+wm_status wm_draft_step(const wm_ring *ring, const wm_mem *mem, const void *k_new, const void *v_new,
+                        const void *q, int32_t n_q_heads, float scale, int32_t n_split, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Operations for wm_workspace_size / wm_plan_splits. */
 #define WM_OP_DRAFT 0
 #define WM_OP_VERIFY 1
 #define WM_OP_DRAFT_STEP 2
+#define WM_OP_DRAFT_MEM 3 /* draft with memory slots, fused or not */
 
 /*
  * Number of key splits an attention call will use, for a cache holding up to
@@ -264,8 +318,10 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
 
 /*
  * Workspace bytes an attention call needs for the same arguments (0 when it
- * runs unsplit; never 0 for WM_OP_DRAFT_STEP).  For WM_OP_DRAFT and
- * WM_OP_DRAFT_STEP pass n_q = 1 and max_keys = sink + window;
+ * runs unsplit; never 0 for WM_OP_DRAFT_STEP and WM_OP_DRAFT_MEM, which cover
+ * the fused step).  For WM_OP_DRAFT and WM_OP_DRAFT_STEP pass n_q = 1 and
+ * max_keys = sink + window; for WM_OP_DRAFT_MEM n_q = 1 and max_keys =
+ * 64 * ceil((sink + window) / 64) + memory capacity;
  * for WM_OP_VERIFY, max_keys = n_cap (contiguous) or max_pages * page_size.
  * Returns (size_t)-1 on invalid arguments.
  */

@@ -91,6 +91,7 @@ __device__ __forceinline__ void report_error(int32_t *err, int32_t code) {
 template <int D, int MT, bool STEP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2,
                 const AttnParams p) {
     using C = AttnCfg<D>;
     using L = AttnSmem<D, MT>;
@@ -129,6 +130,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             seen = STEP ? -1 : 0;  // STEP: nothing is appended, every key is masked
         }
         n_keys = p.n_slots;
+        if (p.mem_count) {  // memory slots follow the ring's (tile-rounded) slots
+            int64_t mc = p.mem_count[b];
+            if (mc < 0 || mc > p.mem_cap) {
+                if (threadIdx.x == 0) report_error(p.err, WM_DEVERR_BAD_LENGTH);
+                mc = mc < 0 ? 0 : p.mem_cap;
+            }
+            n_keys = p.mem_base + mc;
+        }
         qpos0 = STEP ? seen : seen - 1;
         if (STEP && seen >= 0) new_slot = seen < p.sink ? seen : p.sink + (seen - p.sink) % p.window;
     } else {
@@ -155,10 +164,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // =========================================================== producer warp
+    // Keys at or beyond mem_lo are memory slots (always visible to the query).
+    const int64_t mem_lo = p.mem_count ? p.mem_base : INT64_MAX;
     if (warp == C::NW) {
         if (lane == 0 && n_tiles > 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
+            const bool mem_tiles = k_end > mem_lo;
+            if (k_begin < mem_lo) {
+                prefetch_tensormap(&tmk);
+                prefetch_tensormap(&tmv);
+            }
+            if (mem_tiles) {
+                prefetch_tensormap(&tmk2);
+                prefetch_tensormap(&tmv2);
+            }
             // The cache is streamed once per call; the ring is read again by the
             // next draft step, so its lines keep normal priority.
             const uint64_t policy =
@@ -184,18 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     c_row = (int)(key0 % p.page_size);
                     c_outer = page;
                 } else {
-                    c_row = (int)key0;
+                    c_row = (int)(key0 >= mem_lo ? key0 - mem_lo : key0);  // a tile is all ring or all memory
                     c_outer = b;
                 }
+                const CUtensorMap *mk = key0 >= mem_lo ? &tmk2 : &tmk;
+                const CUtensorMap *mv = key0 >= mem_lo ? &tmv2 : &tmv;
                 const uint32_t sK = sbase + s * C::STAGE_BYTES;
                 const uint32_t sV = sK + C::TILE_BYTES;
                 mbar_arrive_expect_tx(bar_full + 8 * s, C::STAGE_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d(sK + c * (TK * 128), &tmk, bar_full + 8 * s, c * 64, c_row, kvh, c_outer,
-                                policy);
-                    tma_load_4d(sV + c * (TK * 128), &tmv, bar_full + 8 * s, c * 64, c_row, kvh, c_outer,
-                                policy);
+                    tma_load_4d(sK + c * (TK * 128), mk, bar_full + 8 * s, c * 64, c_row, kvh, c_outer, policy);
+                    tma_load_4d(sV + c * (TK * 128), mv, bar_full + 8 * s, c * 64, c_row, kvh, c_outer, policy);
                 }
                 issued = t + 1;
             }
@@ -267,10 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
-                tg[n][e] = (tags && kabs < k_end) ? __ldg(tags + kabs) : -1;
+                tg[n][e] = (tags && kabs < k_end && kabs < p.n_slots) ? __ldg(tags + kabs) : -1;
             }
         const int64_t kl = key0 + warp * C::KPW + lane;
-        tg1 = (tags && lane < C::KPW && kl < k_end) ? __ldg(tags + kl) : -1;
+        tg1 = (tags && lane < C::KPW && kl < k_end && kl < p.n_slots) ? __ldg(tags + kl) : -1;
     };
     auto tag_ok = [&](int64_t tg) {
         return tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
                 bool ok = kabs < k_end;
-                if (ok && tags) ok = tag_ok(tag_of(kabs, tg_cur[n][e]));
+                if (ok && tags) ok = kabs >= mem_lo || tag_ok(tag_of(kabs, tg_cur[n][e]));
                 key_ok[n][e] = ok;
             }
 #pragma unroll
@@ -378,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < C::KPW) {
                 const int64_t kabs = key0 + warp * C::KPW + lane;
                 ok_all = kabs < k_end;
-                if (ok_all && tags) ok_all = tag_ok(tag_of(kabs, tg1_cur));
+                if (ok_all && tags) ok_all = kabs >= mem_lo || tag_ok(tag_of(kabs, tg1_cur));
             }
             uint32_t bad = ~__ballot_sync(0xffffffffu, ok_all) & ((1u << C::KPW) - 1u);
             if (bad) {
@@ -546,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, int MT>
-cudaError_t launch_attn_mt(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
-                           cudaStream_t stream) {
+cudaError_t launch_attn_mt(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const AttnParams &p, cudaStream_t stream) {
     constexpr int smem = AttnSmem<D, MT>::TOTAL;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -560,11 +578,12 @@ cudaError_t launch_attn_mt(const CUtensorMap &k, const CUtensorMap &v, const Att
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    return launch_pdl(attn_kernel<D, MT, false>, grid, dim3(kThreads), smem, stream, k, v, p);
+    return launch_pdl(attn_kernel<D, MT, false>, grid, dim3(kThreads), smem, stream, k, v, mk, mv, p);
 }
 
 template <int D, int MT>
-cudaError_t launch_step_mt(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, cudaStream_t stream) {
+cudaError_t launch_step_mt(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const AttnParams &p, cudaStream_t stream) {
     constexpr int smem = AttnSmem<D, MT>::TOTAL;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -577,17 +596,17 @@ cudaError_t launch_step_mt(const CUtensorMap &k, const CUtensorMap &v, const Att
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    return launch_pdl(attn_kernel<D, MT, true>, grid, dim3(kThreads), smem, stream, k, v, p);
+    return launch_pdl(attn_kernel<D, MT, true>, grid, dim3(kThreads), smem, stream, k, v, mk, mv, p);
 }
 
 template <int D>
-cudaError_t launch_attn(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                        cudaStream_t stream) {
+cudaError_t launch_attn(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk, const CUtensorMap &mv,
+                        const AttnParams &p, int m_tiles, cudaStream_t stream) {
     switch (m_tiles) {
-        case 1: return launch_attn_mt<D, 1>(k, v, p, stream);
-        case 2: return launch_attn_mt<D, 2>(k, v, p, stream);
-        case 3: return launch_attn_mt<D, 3>(k, v, p, stream);
-        case 4: return launch_attn_mt<D, 4>(k, v, p, stream);
+        case 1: return launch_attn_mt<D, 1>(k, v, mk, mv, p, stream);
+        case 2: return launch_attn_mt<D, 2>(k, v, mk, mv, p, stream);
+        case 3: return launch_attn_mt<D, 3>(k, v, mk, mv, p, stream);
+        case 4: return launch_attn_mt<D, 4>(k, v, mk, mv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -621,13 +640,13 @@ int blocks_per_sm(int m_tiles, bool step) {
 }
 
 template <int D>
-cudaError_t launch_step(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                        cudaStream_t stream) {
+cudaError_t launch_step(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk, const CUtensorMap &mv,
+                        const AttnParams &p, int m_tiles, cudaStream_t stream) {
     switch (m_tiles) {
-        case 1: return launch_step_mt<D, 1>(k, v, p, stream);
-        case 2: return launch_step_mt<D, 2>(k, v, p, stream);
-        case 3: return launch_step_mt<D, 3>(k, v, p, stream);
-        case 4: return launch_step_mt<D, 4>(k, v, p, stream);
+        case 1: return launch_step_mt<D, 1>(k, v, mk, mv, p, stream);
+        case 2: return launch_step_mt<D, 2>(k, v, mk, mv, p, stream);
+        case 3: return launch_step_mt<D, 3>(k, v, mk, mv, p, stream);
+        case 4: return launch_step_mt<D, 4>(k, v, mk, mv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
 
 #include "wm_internal.h"
@@ -152,17 +153,25 @@ size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
     return o_aligned + (size_t)rows_total * n_split * sizeof(float);
 }
 
-cudaError_t launch_attn_any(int op, const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
+// maps: K and V of the cache or ring, then K and V of the memory-slot store
+// (the same two again when there is none).
+cudaError_t launch_attn_any(int op, const CUtensorMap (&maps)[4], const AttnParams &p, bool step,
                             cudaStream_t st) {
     const int m_tiles = (p.rows + 15) / 16;
-    if (use_tc_kernel(op, p.head_dim)) {
-        return p.head_dim == 128 ? launch_attn_tc_d128(k, v, p, 16 * m_tiles, st)
-                                 : launch_attn_tc_d256(k, v, p, 16 * m_tiles, st);
+    if (!step && use_tc_kernel(op, p.head_dim)) {
+        return p.head_dim == 128 ? launch_attn_tc_d128(maps[0], maps[1], p, 16 * m_tiles, st)
+                                 : launch_attn_tc_d256(maps[0], maps[1], p, 16 * m_tiles, st);
     }
     switch (p.head_dim) {
-        case 64: return launch_attn_d64(k, v, p, m_tiles, st);
-        case 128: return launch_attn_d128(k, v, p, m_tiles, st);
-        case 256: return launch_attn_d256(k, v, p, m_tiles, st);
+        case 64:
+            return step ? launch_step_d64(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st)
+                        : launch_attn_d64(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st);
+        case 128:
+            return step ? launch_step_d128(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st)
+                        : launch_attn_d128(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st);
+        case 256:
+            return step ? launch_step_d256(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st)
+                        : launch_attn_d256(maps[0], maps[1], maps[2], maps[3], p, m_tiles, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -194,6 +203,18 @@ wm_status kv_check(const wm_kv *kv, bool need_tile_pages) {
 
 wm_status launch_status(cudaError_t e) { return e == cudaSuccess ? WM_OK : WM_ERR_CUDA; }
 
+bool mem_ok(const wm_mem *m) {
+    return m && m->k && m->v && m->count && m->batch > 0 && m->n_kv_heads > 0 && head_dim_ok(m->head_dim) &&
+           m->capacity > 0 && m->capacity <= INT32_MAX / 2 && aligned(m->k, 16) && aligned(m->v, 16) &&
+           aligned(m->count, 8);
+}
+
+// First key index of the memory region: the ring's slots rounded up to whole
+// 64-key tiles, so that every tile is all ring or all memory.
+int64_t mem_base_of(const wm_ring *ring) {
+    return ((int64_t)ring->sink + ring->window + kKeyTile - 1) / kKeyTile * kKeyTile;
+}
+
 }  // namespace
 }  // namespace wm
 
@@ -217,12 +238,13 @@ int32_t wm_version(void) { return 100; }
 
 int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
                        int32_t head_dim, int64_t max_keys, int32_t n_split) {
-    if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY && op != WM_OP_DRAFT_STEP) || batch <= 0 || n_kv_heads <= 0 ||
+    if ((op != WM_OP_DRAFT && op != WM_OP_VERIFY && op != WM_OP_DRAFT_STEP && op != WM_OP_DRAFT_MEM) || batch <= 0 ||
+        n_kv_heads <= 0 ||
         n_q_heads <= 0 || n_q <= 0 || !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
         return 0;
-    if (op == WM_OP_DRAFT_STEP) {
+    if (op == WM_OP_DRAFT_STEP || op == WM_OP_DRAFT_MEM) {
         if (n_q != 1) return 0;
-        op = WM_OP_DRAFT;  // the fused step splits exactly as the draft attention does
+        op = WM_OP_DRAFT;  // all draft forms split alike
     }
     return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim,
                        ctas_per_sm(op, head_dim, n_q * (n_q_heads / n_kv_heads)))
@@ -233,7 +255,7 @@ size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t 
                          int32_t head_dim, int64_t max_keys, int32_t n_split) {
     const int32_t ns = wm_plan_splits(op, batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split);
     if (ns <= 0) return (size_t)-1;
-    if (op == WM_OP_DRAFT_STEP)  // partials even when unsplit: the merge commits the append
+    if (op == WM_OP_DRAFT_STEP || op == WM_OP_DRAFT_MEM)  // partials even when unsplit (fused step)
         return partial_bytes((int64_t)batch * n_q_heads, ns, head_dim);
     if (ns == 1) return 0;
     return partial_bytes((int64_t)batch * n_q * n_q_heads, ns, head_dim);
@@ -305,14 +327,19 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
                                           static_cast<cudaStream_t>(stream)));
 }
 
-// Shared tail of the two attention entry points: plan, check the workspace,
-// launch the attention kernel and (if split) the merge.
-static wm_status run_attention(int op, AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                               int64_t max_keys, int32_t n_split, void *out, float *lse, void *ws,
-                               size_t ws_bytes, cudaStream_t st) {
-    const SplitPlan pl =
-        plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim), p.head_dim,
-                    ctas_per_sm(op, p.head_dim, p.rows));
+// Shared tail of the attention entry points: plan, check the workspace,
+// launch the attention kernel and (if split, or always for the fused step)
+// the merge -- which for the fused step also commits n_seen.
+// encode_maps fills the four tensor maps; it runs after every host-side check
+// (so that a bad argument is reported before any CUDA or driver call).
+using MapEncoder = std::function<bool(CUtensorMap (&)[4])>;
+
+static wm_status run_attention(int op, AttnParams &p, const MapEncoder &encode_maps, int64_t max_keys,
+                               int32_t n_split, void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
+                               int64_t *commit_n_seen = nullptr) {
+    const bool step = commit_n_seen != nullptr;
+    const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim),
+                                     p.head_dim, ctas_per_sm(op, p.head_dim, p.rows));
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
     p.n_split = pl.n_split;
     p.keys_per_split = pl.keys_per_split;
@@ -320,87 +347,56 @@ static wm_status run_attention(int op, AttnParams &p, const CUtensorMap &mk, con
     p.lse = lse;
     p.o_part = nullptr;
     p.lse_part = nullptr;
-    if (pl.n_split > 1) {
+    const bool partials = pl.n_split > 1 || step;
+    if (partials) {
         const size_t need = partial_bytes(rows_total, pl.n_split, p.head_dim);
         if (!ws || ws_bytes < need || !aligned(ws, 256)) return WM_ERR_WORKSPACE;
         const size_t o = (size_t)rows_total * pl.n_split * p.head_dim * sizeof(float);
         p.o_part = static_cast<float *>(ws);
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + ((o + 255) & ~(size_t)255));
     }
-    cudaError_t e = launch_attn_any(op, mk, mv, p, st);
+    p.err = device_error_ptr();
+    if (!p.err) return WM_ERR_CUDA;
+    CUtensorMap maps[4];
+    if (!encode_maps(maps)) return WM_ERR_CUDA;
+    cudaError_t e = launch_attn_any(op, maps, p, step, st);
     if (e != cudaSuccess) return WM_ERR_CUDA;
-    if (pl.n_split > 1) {
-        e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, nullptr, 0, st);
+    if (partials) {
+        e = launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, p.head_dim, out, lse, commit_n_seen,
+                             p.n_q * p.n_q_heads, st);
         if (e != cudaSuccess) return WM_ERR_CUDA;
     }
     return WM_OK;
 }
 
-wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
-                        void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+// Validation and parameters shared by the draft calls (plain, with memory
+// slots, fused with the append).  On success fills p (ring and, if mem, the
+// memory region), the tensor-map encoder and the key count to plan over.
+static wm_status draft_setup(const wm_ring *ring, const wm_mem *mem, const void *q, int32_t n_q_heads,
+                             float scale, int32_t n_split, void *out, float *lse, AttnParams &p,
+                             MapEncoder &maps, int64_t &plan_keys) {
     if (!ring_ok(ring) || !q || !out || n_q_heads <= 0 || n_split < 0 || !std::isfinite(scale))
         return WM_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return WM_ERR_INVALID_ARG;
     if (n_q_heads % ring->n_kv_heads) return WM_ERR_INVALID_ARG;
-    const int group = n_q_heads / ring->n_kv_heads;
-    if (group > kMaxRows) return WM_ERR_UNSUPPORTED;
-    int32_t *err = device_error_ptr();
-    if (!err) return WM_ERR_CUDA;
-    const int n_slots = ring->sink + ring->window;
-    const int box = key_tile(WM_OP_DRAFT, ring->head_dim);
-    CUtensorMap mk, mv;
-    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box) ||
-        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, box))
-        return WM_ERR_CUDA;
-    AttnParams p;
-    std::memset(&p, 0, sizeof p);
-    p.source = KEYS_RING;
-    p.batch = ring->batch;
-    p.n_kv_heads = ring->n_kv_heads;
-    p.head_dim = ring->head_dim;
-    p.pos_tag = ring->pos_tag;
-    p.n_seen = ring->n_seen;
-    p.n_slots = n_slots;
-    p.sink = ring->sink;
-    p.window = ring->window;
-    p.capacity = n_slots;
-    p.box_rows = box;
-    p.q = q;
-    p.n_q = 1;
-    p.n_q_heads = n_q_heads;
-    p.group = group;
-    p.rows = group;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.err = err;
-    return run_attention(WM_OP_DRAFT, p, mk, mv, n_slots, n_split, out, lse, workspace, workspace_bytes,
-                         static_cast<cudaStream_t>(stream));
-}
-
-wm_status wm_draft_step(const wm_ring *ring, const void *k_new, const void *v_new, const void *q,
-                        int32_t n_q_heads, float scale, int32_t n_split, void *out, float *lse, void *workspace,
-                        size_t workspace_bytes, void *stream) {
-    if (!ring_ok(ring) || !k_new || !v_new || !q || !out || n_q_heads <= 0 || n_split < 0 ||
-        !std::isfinite(scale))
+    if (mem && (!mem_ok(mem) || mem->batch != ring->batch || mem->n_kv_heads != ring->n_kv_heads ||
+                mem->head_dim != ring->head_dim))
         return WM_ERR_INVALID_ARG;
-    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16) ||
-        (lse && !aligned(lse, 4)))
-        return WM_ERR_INVALID_ARG;
-    if (n_q_heads % ring->n_kv_heads) return WM_ERR_INVALID_ARG;
     const int group = n_q_heads / ring->n_kv_heads;
     if (group > kMaxRows) return WM_ERR_UNSUPPORTED;
     const int n_slots = ring->sink + ring->window;
-    const SplitPlan pl = plan_splits(ring->batch * ring->n_kv_heads, ring->batch, n_slots, n_split, kKeyTile,
-                                     ring->head_dim, ctas_per_sm(WM_OP_DRAFT, ring->head_dim, group));
-    const int64_t rows_total = (int64_t)ring->batch * n_q_heads;
-    const size_t need = partial_bytes(rows_total, pl.n_split, ring->head_dim);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return WM_ERR_WORKSPACE;
-    int32_t *err = device_error_ptr();
-    if (!err) return WM_ERR_CUDA;
-    CUtensorMap mk, mv;
-    if (!encode_kv_map(&mk, ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile) ||
-        !encode_kv_map(&mv, ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile))
-        return WM_ERR_CUDA;
-    AttnParams p;
+    maps = [ring, mem, n_slots](CUtensorMap (&m)[4]) {
+        if (!encode_kv_map(&m[0], ring->k, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile) ||
+            !encode_kv_map(&m[1], ring->v, ring->head_dim, n_slots, ring->n_kv_heads, ring->batch, kKeyTile))
+            return false;
+        if (!mem) {
+            m[2] = m[0];
+            m[3] = m[1];
+            return true;
+        }
+        return encode_kv_map(&m[2], mem->k, mem->head_dim, mem->capacity, mem->n_kv_heads, mem->batch, kKeyTile) &&
+               encode_kv_map(&m[3], mem->v, mem->head_dim, mem->capacity, mem->n_kv_heads, mem->batch, kKeyTile);
+    };
     std::memset(&p, 0, sizeof p);
     p.source = KEYS_RING;
     p.batch = ring->batch;
@@ -419,30 +415,72 @@ wm_status wm_draft_step(const wm_ring *ring, const void *k_new, const void *v_ne
     p.group = group;
     p.rows = group;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.n_split = pl.n_split;
-    p.keys_per_split = pl.keys_per_split;
-    p.out = out;
-    p.lse = lse;
-    const size_t o_bytes = (size_t)rows_total * pl.n_split * ring->head_dim * sizeof(float);
-    p.o_part = static_cast<float *>(workspace);
-    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + ((o_bytes + 255) & ~(size_t)255));
-    p.err = err;
+    plan_keys = n_slots;
+    if (mem) {
+        p.mem_count = mem->count;
+        p.mem_cap = mem->capacity;
+        p.mem_base = mem_base_of(ring);
+        plan_keys = p.mem_base + mem->capacity;
+    }
+    return WM_OK;
+}
+
+wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
+                        void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    AttnParams p;
+    MapEncoder maps;
+    int64_t keys = 0;
+    const wm_status s = draft_setup(ring, nullptr, q, n_q_heads, scale, n_split, out, lse, p, maps, keys);
+    if (s != WM_OK) return s;
+    return run_attention(WM_OP_DRAFT, p, maps, keys, n_split, out, lse, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+wm_status wm_draft_attn_mem(const wm_ring *ring, const wm_mem *mem, const void *q, int32_t n_q_heads, float scale,
+                            int32_t n_split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    if (!mem) return WM_ERR_INVALID_ARG;
+    AttnParams p;
+    MapEncoder maps;
+    int64_t keys = 0;
+    const wm_status s = draft_setup(ring, mem, q, n_q_heads, scale, n_split, out, lse, p, maps, keys);
+    if (s != WM_OK) return s;
+    return run_attention(WM_OP_DRAFT, p, maps, keys, n_split, out, lse, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+wm_status wm_draft_step(const wm_ring *ring, const wm_mem *mem, const void *k_new, const void *v_new,
+                        const void *q, int32_t n_q_heads, float scale, int32_t n_split, void *out, float *lse,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return WM_ERR_INVALID_ARG;
+    AttnParams p;
+    MapEncoder maps;
+    int64_t keys = 0;
+    const wm_status s = draft_setup(ring, mem, q, n_q_heads, scale, n_split, out, lse, p, maps, keys);
+    if (s != WM_OK) return s;
     p.k_new = k_new;
     p.v_new = v_new;
     p.ring_k = ring->k;
     p.ring_v = ring->v;
     p.tag_w = ring->pos_tag;
-    const int m_tiles = (group + 15) / 16;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (ring->head_dim) {
-        case 64: e = launch_step_d64(mk, mv, p, m_tiles, st); break;
-        case 128: e = launch_step_d128(mk, mv, p, m_tiles, st); break;
-        default: e = launch_step_d256(mk, mv, p, m_tiles, st); break;
-    }
-    if (e != cudaSuccess) return WM_ERR_CUDA;
-    return launch_status(launch_lse_merge(p.o_part, p.lse_part, pl.n_split, rows_total, ring->head_dim, out, lse,
-                                          ring->n_seen, n_q_heads, st));
+    return run_attention(WM_OP_DRAFT, p, maps, keys, n_split, out, lse, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream), ring->n_seen);
+}
+
+wm_status wm_mem_append(const wm_mem *mem, const void *k_new, const void *v_new, void *stream) {
+    if (!mem_ok(mem) || !k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return WM_ERR_INVALID_ARG;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    return launch_status(launch_mem_append(mem->k, mem->v, mem->count, mem->capacity, mem->batch, mem->n_kv_heads,
+                                           mem->head_dim, k_new, v_new, err, static_cast<cudaStream_t>(stream)));
+}
+
+wm_status wm_mem_rollback(const wm_mem *mem, const int64_t *new_count, void *stream) {
+    if (!mem_ok(mem) || !new_count || !aligned(new_count, 8)) return WM_ERR_INVALID_ARG;
+    int32_t *err = device_error_ptr();
+    if (!err) return WM_ERR_CUDA;
+    return launch_status(
+        launch_mem_rollback(mem->count, mem->batch, new_count, err, static_cast<cudaStream_t>(stream)));
 }
 
 wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_q_heads, float scale,
@@ -456,18 +494,20 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     if (n_q_heads % kv->n_kv_heads) return WM_ERR_INVALID_ARG;
     const int group = n_q_heads / kv->n_kv_heads;
     if ((int64_t)group * n_q > kMaxRows) return WM_ERR_UNSUPPORTED;
-    int32_t *err = device_error_ptr();
-    if (!err) return WM_ERR_CUDA;
     const bool paged = kv->block_table != nullptr;
     const int64_t capacity = paged ? (int64_t)kv->max_pages * kv->page_size : kv->n_cap;
-    CUtensorMap mk, mv;
     const int64_t inner = paged ? kv->page_size : kv->n_cap;
     const int64_t outer = paged ? kv->n_pages : kv->batch;
     const int tile = key_tile(WM_OP_VERIFY, kv->head_dim);
     const int box = paged && kv->page_size % tile ? kKeyTile : tile;  // a box never crosses a page
-    if (!encode_kv_map(&mk, kv->k, kv->head_dim, inner, kv->n_kv_heads, outer, box) ||
-        !encode_kv_map(&mv, kv->v, kv->head_dim, inner, kv->n_kv_heads, outer, box))
-        return WM_ERR_CUDA;
+    const MapEncoder maps = [kv, inner, outer, box](CUtensorMap (&m)[4]) {
+        if (!encode_kv_map(&m[0], kv->k, kv->head_dim, inner, kv->n_kv_heads, outer, box) ||
+            !encode_kv_map(&m[1], kv->v, kv->head_dim, inner, kv->n_kv_heads, outer, box))
+            return false;
+        m[2] = m[0];
+        m[3] = m[1];
+        return true;
+    };
     AttnParams p;
     std::memset(&p, 0, sizeof p);
     p.source = paged ? KEYS_PAGED : KEYS_CONTIG;
@@ -487,8 +527,7 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     p.group = group;
     p.rows = group * n_q;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.err = err;
-    return run_attention(WM_OP_VERIFY, p, mk, mv, capacity, n_split, out, lse, workspace, workspace_bytes,
+    return run_attention(WM_OP_VERIFY, p, maps, capacity, n_split, out, lse, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
 }
 

@@ -68,15 +68,21 @@ struct AttnParams {
     void *ring_k;         // the ring's K and V, written at slot(p)
     void *ring_v;
     int32_t *tag_w;       // writable pos_tag of the ring
+    // memory slots (memory-augmented draft): keys mem_base .. mem_base + count[b] - 1
+    // are slots 0 .. count[b] - 1, read through the second pair of tensor maps
+    const int64_t *mem_count;  // [B]; NULL: no memory slots
+    int64_t mem_cap;           // slots the memory store holds per (sequence, KV head)
+    int64_t mem_base;          // first key index of the memory region (ring tiles x 64)
 };
 
-// Launch the attention kernel for head dim D (defined in attn_d<D>.cu).
-cudaError_t launch_attn_d64(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
-                            int m_tiles, cudaStream_t stream);
-cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
-                             int m_tiles, cudaStream_t stream);
-cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
-                             int m_tiles, cudaStream_t stream);
+// Launch the attention kernel for head dim D (defined in attn_d<D>.cu).  mk/mv
+// map the memory-slot store when p.mem_count is set (else any valid maps).
+cudaError_t launch_attn_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                            const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
+cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                             const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
+cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                             const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
 
 // Resident CTAs per SM of the mma.sync attention kernel for head dim D with
 // m_tiles row tiles (step: the fused draft-step instance); 0 if unknown.
@@ -86,12 +92,12 @@ int attn_blocks_per_sm_d256(int m_tiles, bool step);
 
 // Fused draft step (ring append + draft attention) for head dim D; always
 // writes split partials (o_part / lse_part) for the merge kernel.
-cudaError_t launch_step_d64(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                            cudaStream_t stream);
-cudaError_t launch_step_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                             cudaStream_t stream);
-cudaError_t launch_step_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int m_tiles,
-                             cudaStream_t stream);
+cudaError_t launch_step_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                            const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
+cudaError_t launch_step_d128(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                             const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
+cudaError_t launch_step_d256(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                             const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
 
 // Tensor-core (tcgen05) attention kernel for head dims 128 and 256 (attn_tc_d<D>.cu);
 // n_rows16 is the row count per KV head rounded up to 16, 128-key tiles.
@@ -121,6 +127,14 @@ struct HistSource {
 cudaError_t launch_ring_fill(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
                              int n_kv_heads, int head_dim, int sink, int window,
                              const HistSource &hist, int32_t *err, cudaStream_t stream);
+
+// Memory-slot store of the memory-augmented draft (mem.cu): append one slot per
+// sequence at count[b], and truncate the counts.
+cudaError_t launch_mem_append(void *mk, void *mv, int64_t *count, int64_t capacity, int batch, int n_kv_heads,
+                              int head_dim, const void *k_new, const void *v_new, int32_t *err,
+                              cudaStream_t stream);
+cudaError_t launch_mem_rollback(int64_t *count, int batch, const int64_t *new_count, int32_t *err,
+                                cudaStream_t stream);
 
 cudaError_t launch_ring_rollback(int32_t *tag, int64_t *n_seen, int batch, int n_slots,
                                  const int64_t *new_len, int32_t *err, cudaStream_t stream);

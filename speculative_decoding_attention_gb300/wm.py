@@ -17,12 +17,13 @@ import torch
 from . import build as _build
 
 WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, WM_ERR_DEVICE_DATA = range(6)
-WM_OP_DRAFT, WM_OP_VERIFY, WM_OP_DRAFT_STEP = 0, 1, 2
+WM_OP_DRAFT, WM_OP_VERIFY, WM_OP_DRAFT_STEP, WM_OP_DRAFT_MEM = 0, 1, 2, 3
 DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout", 4: "internal check"}
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
-            "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step")
+            "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step", "wm_draft_attn_mem",
+            "wm_mem_append", "wm_mem_rollback")
 STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
 
 _lib = None
@@ -39,6 +40,12 @@ class _Ring(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("pos_tag", ctypes.c_void_p),
                 ("n_seen", ctypes.c_void_p), ("batch", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("sink", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class _Mem(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("count", ctypes.c_void_p),
+                ("capacity", ctypes.c_int64), ("batch", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
 
 
 class _KV(ctypes.Structure):
@@ -69,7 +76,10 @@ def load() -> ctypes.CDLL:
         lib.wm_draft_attn.argtypes = [P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_verify_attn.argtypes = [P, P, I32, I32, F, I32, P, P, P, ctypes.c_size_t, P]
         lib.wm_draft_attn_static.argtypes = [P, P, I32, F, I32, P, P, P]
-        lib.wm_draft_step.argtypes = [P, P, P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
+        lib.wm_draft_step.argtypes = [P, P, P, P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
+        lib.wm_draft_attn_mem.argtypes = [P, P, P, I32, F, I32, P, P, P, ctypes.c_size_t, P]
+        lib.wm_mem_append.argtypes = [P, P, P, P]
+        lib.wm_mem_rollback.argtypes = [P, P, P]
         lib.wm_lse_merge.argtypes = [P, P, I32, I64, I32, P, P, P]
         lib.wm_plan_splits.argtypes = [I32, I32, I32, I32, I32, I32, I64, I32]
         lib.wm_plan_splits.restype = I32
@@ -152,6 +162,38 @@ class Ring:
         r.batch, r.n_kv_heads, r.head_dim = self.batch, self.n_kv_heads, self.head_dim
         r.sink, r.window = self.sink, self.window
         return r
+
+
+@dataclass
+class Mem:
+    """Memory slots of a memory-augmented draft (``wm_mem``): K/V
+    [B, Hkv, capacity, D] bf16 and the per-sequence count of materialized slots."""
+    k: torch.Tensor
+    v: torch.Tensor
+    count: torch.Tensor      # [B] int64
+
+    @classmethod
+    def create(cls, batch: int, n_kv_heads: int, head_dim: int, capacity: int, device="cuda") -> "Mem":
+        k = torch.zeros((batch, n_kv_heads, capacity, head_dim), dtype=torch.bfloat16, device=device)
+        return cls(k, torch.zeros_like(k), torch.zeros((batch,), dtype=torch.int64, device=device))
+
+    @property
+    def capacity(self) -> int:
+        return self.k.shape[2]
+
+    def c(self) -> _Mem:
+        m = _Mem()
+        m.k = _dev(self.k, torch.bfloat16, "mem.k")
+        m.v = _dev(self.v, torch.bfloat16, "mem.v")
+        m.count = _dev(self.count, torch.int64, "mem.count")
+        m.capacity = self.capacity
+        m.batch, m.n_kv_heads, m.head_dim = self.k.shape[0], self.k.shape[1], self.k.shape[3]
+        return m
+
+
+def mem_keys(ring: "Ring", mem: Mem) -> int:
+    """max_keys of WM_OP_DRAFT_MEM: the ring's slots in whole 64-key tiles plus the memory capacity."""
+    return -(-(ring.sink + ring.window) // 64) * 64 + mem.capacity
 
 
 @dataclass
@@ -268,33 +310,75 @@ def draft_attn(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=
     return out, lse
 
 
-def step_workspace(ring: Ring, n_q_heads: int, n_split: int = 0, device=None) -> torch.Tensor:
-    """A workspace for draft_step on this ring (split partials; never empty)."""
-    need = workspace_size(WM_OP_DRAFT_STEP, ring.batch, ring.n_kv_heads, n_q_heads, 1, ring.head_dim,
-                          ring.sink + ring.window, n_split)
+def step_workspace(ring: Ring, n_q_heads: int, n_split: int = 0, device=None, mem: Mem | None = None
+                   ) -> torch.Tensor:
+    """A workspace for draft_step (or draft_attn_mem) on this ring (split
+    partials; never empty)."""
+    if mem is None:
+        need = workspace_size(WM_OP_DRAFT_STEP, ring.batch, ring.n_kv_heads, n_q_heads, 1, ring.head_dim,
+                              ring.sink + ring.window, n_split)
+    else:
+        need = workspace_size(WM_OP_DRAFT_MEM, ring.batch, ring.n_kv_heads, n_q_heads, 1, ring.head_dim,
+                              mem_keys(ring, mem), n_split)
     return torch.empty(need, dtype=torch.uint8, device=device if device is not None else ring.k.device)
 
 
 def draft_step(ring: Ring, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, scale: float,
-               workspace: torch.Tensor, n_split: int = 0, out=None, lse=None, stream=None):
+               workspace: torch.Tensor, n_split: int = 0, out=None, lse=None, stream=None, mem: Mem | None = None):
     """Fused ring append + draft attention: append (k_new, v_new) [B, Hkv, D]
     at p = n_seen[b] and attend q [B, Hq, D] from position p over the sinks and
     the window, in one attention launch (plus the split merge, which commits
     n_seen).  ``workspace`` comes from step_workspace().  Returns (out bf16,
-    lse fp32), bit-identical to ring_append followed by draft_attn."""
+    lse fp32), bit-identical to ring_append followed by draft_attn (draft_attn_mem
+    when ``mem`` is given: the query then also attends to the memory slots)."""
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     r = ring.c()
-    _check(load().wm_draft_step(ctypes.byref(r), _dev(k_new, torch.bfloat16, "k_new"),
+    m = mem.c() if mem is not None else None
+    _check(load().wm_draft_step(ctypes.byref(r), ctypes.byref(m) if m is not None else None,
+                                _dev(k_new, torch.bfloat16, "k_new"),
                                 _dev(v_new, torch.bfloat16, "v_new"), _dev(q, torch.bfloat16, "q"), Hq,
                                 float(scale), n_split, _dev(out, torch.bfloat16, "out"),
                                 _dev(lse, torch.float32, "lse"), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "wm_draft_step")
     return out, lse
+
+
+def draft_attn_mem(ring: Ring, mem: Mem, q: torch.Tensor, scale: float, n_split: int = 0, out=None, lse=None,
+                   workspace=None, stream=None):
+    """Draft attention over the sinks, the window and the memory slots
+    0..mem.count[b]-1 (memory-augmented draft); returns (out bf16, lse fp32)."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = workspace_size(WM_OP_DRAFT_MEM, B, ring.n_kv_heads, Hq, 1, D, mem_keys(ring, mem), n_split)
+    ws, ws_bytes = _workspace(need, q.device, workspace)
+    r, m = ring.c(), mem.c()
+    _check(load().wm_draft_attn_mem(ctypes.byref(r), ctypes.byref(m), _dev(q, torch.bfloat16, "q"), Hq,
+                                    float(scale), n_split, _dev(out, torch.bfloat16, "out"),
+                                    _dev(lse, torch.float32, "lse"), ws, ws_bytes, _stream(stream)),
+           "wm_draft_attn_mem")
+    return out, lse
+
+
+def mem_append(mem: Mem, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Materialize one memory slot per sequence (k_new, v_new: [B, Hkv, D] bf16)."""
+    m = mem.c()
+    _check(load().wm_mem_append(ctypes.byref(m), _dev(k_new, torch.bfloat16, "k_new"),
+                                _dev(v_new, torch.bfloat16, "v_new"), _stream(stream)), "wm_mem_append")
+
+
+def mem_rollback(mem: Mem, new_count: torch.Tensor, stream=None) -> None:
+    """Discard memory slots beyond new_count[b] (int64 [B] device tensor)."""
+    m = mem.c()
+    _check(load().wm_mem_rollback(ctypes.byref(m), _dev(new_count, torch.int64, "new_count"), _stream(stream)),
+           "wm_mem_rollback")
 
 
 def draft_attn_static(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=None, lse=None,

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from speculative_decoding_attention_gb300 import build as wm_build
 from speculative_decoding_attention_gb300 import wm
@@ -116,10 +117,10 @@ def test_draft_step_rejects_bad_arguments(lib):
 
     def call(k_new=P(1 << 23), v_new=P(3 << 22), hq=8, scale=1.0, ws_ptr=ws, ws_bytes=1 << 20, ring=r):
         # an explicit split count: the plan needs no device query
-        return lib.wm_draft_step(ctypes.byref(ring), k_new, v_new, q, hq, scale, 4, out, None, ws_ptr, ws_bytes,
-                                 None)
+        return lib.wm_draft_step(ctypes.byref(ring), None, k_new, v_new, q, hq, scale, 4, out, None, ws_ptr,
+                                 ws_bytes, None)
 
-    assert lib.wm_draft_step(None, P(16), P(16), q, 8, 1.0, 0, out, None, ws, 1 << 20, None) == \
+    assert lib.wm_draft_step(None, None, P(16), P(16), q, 8, 1.0, 0, out, None, ws, 1 << 20, None) == \
         wm.WM_ERR_INVALID_ARG
     assert call(k_new=None) == wm.WM_ERR_INVALID_ARG
     assert call(v_new=P((1 << 23) + 8)) == wm.WM_ERR_INVALID_ARG      # misaligned
@@ -129,6 +130,45 @@ def test_draft_step_rejects_bad_arguments(lib):
     assert call(ws_ptr=None) == wm.WM_ERR_WORKSPACE
     assert call(ws_ptr=P((1 << 26) + 16)) == wm.WM_ERR_WORKSPACE      # not 256-byte aligned
     assert call(ws_bytes=8) == wm.WM_ERR_WORKSPACE
+
+
+def _mem(**over):
+    m = wm._Mem()
+    m.k, m.v, m.count = 5 << 20, 6 << 20, 7 << 20
+    m.capacity, m.batch, m.n_kv_heads, m.head_dim = 64, 1, 2, 128
+    for k, v in over.items():
+        setattr(m, k, v)
+    return m
+
+
+@pytest.mark.parametrize("over", [dict(capacity=0), dict(count=None), dict(head_dim=64), dict(n_kv_heads=4),
+                                  dict(batch=2), dict(k=(5 << 20) + 8)])
+def test_draft_with_memory_rejects_bad_stores(lib, over):
+    r, m = _ring(), _mem(**over)
+    P = ctypes.c_void_p
+    assert lib.wm_draft_attn_mem(ctypes.byref(r), ctypes.byref(m), P(1 << 24), 8, 1.0, 2, P(1 << 25), None,
+                                 P(1 << 26), 1 << 20, None) == wm.WM_ERR_INVALID_ARG
+
+
+def test_memory_store_calls_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    r = _ring()
+    assert lib.wm_draft_attn_mem(ctypes.byref(r), None, P(1 << 24), 8, 1.0, 2, P(1 << 25), None, P(1 << 26),
+                                 1 << 20, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_mem_append(None, P(16), P(16), None) == wm.WM_ERR_INVALID_ARG
+    m = _mem()
+    assert lib.wm_mem_append(ctypes.byref(m), None, P(16), None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_mem_append(ctypes.byref(m), P(16), P(24), None) == wm.WM_ERR_INVALID_ARG  # misaligned
+    assert lib.wm_mem_rollback(ctypes.byref(m), None, None) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_mem_rollback(ctypes.byref(_mem(capacity=-1)), P(16), None) == wm.WM_ERR_INVALID_ARG
+
+
+def test_memory_draft_plans_over_ring_tiles_plus_capacity(lib):
+    # the memory region starts at the ring's slots rounded up to whole 64-key tiles
+    ring = wm.Ring(None, None, None, None, 4, 4096)
+    mem = wm.Mem(torch.empty((1, 2, 300, 8)), None, None)
+    assert wm.mem_keys(ring, mem) == 4160 + 300
+    assert wm.plan_splits(wm.WM_OP_DRAFT_MEM, 1, 2, 16, 1, 256, 4460, 1000) == 70  # 65 + 5 tiles
 
 
 def test_draft_step_workspace(lib):
