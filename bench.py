@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--depth", type=int, default=None, help="draft depth d (verify T = d + 1)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--context", type=int, default=None,
+                    help="shorter context, same recipe (small cases for profiler captures; not a bench line)")
     return ap.parse_args()
 
 
@@ -184,11 +186,11 @@ class ClockSampler:
 class Step:
     """Device state of one workload and its captured step."""
 
-    def __init__(self, w: workloads.Workload, depth: int, device):
+    def __init__(self, w: workloads.Workload, depth: int, device, context: int | None = None):
         from speculative_decoding_attention_gb300 import wm
 
         self.wm, self.w, self.d, self.T, self.dev = wm, w, depth, depth + 1, device
-        self.inp = wm_inputs.make_inputs(w, depth=depth, device=device)
+        self.inp = wm_inputs.make_inputs(w, depth=depth, device=device, context=context)
         inp = self.inp
         self.kv = wm.KVCache(inp.k, inp.v, inp.seq_lens, inp.block_table)
         self.ring = wm.Ring.create(w.batch, w.n_kv_heads, w.head_dim, w.sink, w.window, device)
@@ -283,7 +285,7 @@ def gpu_arm(args, rank, world, local):
     depth = args.depth if args.depth is not None else (
         workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)
 
-    st = Step(w, depth, device)
+    st = Step(w, depth, device, context=args.context)
     st.capture()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
@@ -366,7 +368,8 @@ def gpu_arm(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
         "config": {
             "workload": w.name,
-            "batch": B, "context": w.context if not w.ragged else list(w.ragged),
+            "batch": B, "context": (args.context if args.context else w.context) if not w.ragged else
+            list(st.inp.seq_lens_host),
             "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D, "sink": w.sink, "window": w.window,
             "draft_depth": depth, "verify_positions": st.T, "kv_layout": "paged" if w.page_size else "contiguous",
             "draft_splits": st.d_splits, "verify_splits": st.v_splits,
