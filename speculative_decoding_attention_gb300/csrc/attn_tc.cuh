@@ -54,6 +54,7 @@ constexpr int kTcPageCache = 256;  // block-table entries of one split kept in s
 __host__ __device__ constexpr int tc_softmax_warps(int nr) { return nr <= 32 ? 4 * (nr / 8) : 4 * (nr / 16); }
 __host__ __device__ constexpr int tc_threads(int nr) { return (2 + tc_softmax_warps(nr)) * 32; }
 constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
+constexpr float kMaxFloor = -1e30f;  // running-max start, below any finite logit (log2 units)
 
 template <int D, int NR, int NSLOT_, int NPB_>
 struct TcLayout {
@@ -444,12 +445,19 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             if (lane == 0) mbar_arrive(bar_qfull);
         }
         const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
-        float m_run[HR], l_run[HR];  // running max (same in every thread) and this key-thread's sum
+        // Running max (the same in every thread) and this key-thread's sum.  The
+        // max starts at a finite floor rather than -inf: any visible logit exceeds
+        // it by more than the lazy margin, so the first one raises it before a P
+        // is formed, and 2^(s - m) needs no -inf guard (masked s = -inf gives 0).
+        float m_run[HR], l_run[HR];
 #pragma unroll
         for (int i = 0; i < HR; ++i) {
-            m_run[i] = -CUDART_INF_F;
+            m_run[i] = kMaxFloor;
             l_run[i] = 0.f;
         }
+        // 8-row chunks of this warp's rows that hold real rows (warp-uniform);
+        // padding rows (the MMA's N is a multiple of 16) get P = 0 without work
+        const int live_chunks = min(HR / 8, max(0, (p.rows - r0 + 7) / 8));
 
         for (int t = 0; t < n_tiles; ++t) {
             const int64_t key0 = k_begin + (int64_t)t * TK;
@@ -467,14 +475,14 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             }
             live = !warp_aborted(flags);
             tc::fence_after_sync();  // order the S loads after the MMA completion observed above
+#pragma unroll
+            for (int i = 0; i < HR; ++i) s[i] = -CUDART_INF_F;
             if (live) {
 #pragma unroll
                 for (int c = 0; c < HR / 8; ++c)
-                    tc::ld_32x32b_x8(tmem + lane_off + C::S_COL + (t & 1) * NR + r0 + 8 * c, s + 8 * c);
+                    if (c < live_chunks)
+                        tc::ld_32x32b_x8(tmem + lane_off + C::S_COL + (t & 1) * NR + r0 + 8 * c, s + 8 * c);
                 tc::wait_ld();
-            } else {
-#pragma unroll
-                for (int i = 0; i < HR; ++i) s[i] = -CUDART_INF_F;
             }
             tc::fence_before_sync();
             __syncwarp();
@@ -485,14 +493,26 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             const bool key_tile = tags != nullptr || key0 + TK > k_end;
             const int64_t rel = qpos0 - kabs;  // key visible to row r iff rel + r / group >= 0
             bool need = false;
+            if (key_tile || causal_tile) {
 #pragma unroll
-            for (int i = 0; i < HR; ++i) {
-                bool ok = true;
-                if (key_tile) ok = key_ok;
-                if (causal_tile) ok = ok && rel + (r0 + i) / p.group >= 0;
-                const float v = ok ? s[i] * p.scale_log2 : -CUDART_INF_F;
-                s[i] = v;
-                need |= v > m_run[i] + kLazyRescale;
+                for (int i = 0; i < HR; ++i) {
+                    bool ok = i < 8 * live_chunks;
+                    if (key_tile) ok = ok && key_ok;
+                    if (causal_tile) ok = ok && rel + (r0 + i) / p.group >= 0;
+                    const float v = ok ? s[i] * p.scale_log2 : -CUDART_INF_F;
+                    s[i] = v;
+                    need |= v > m_run[i] + kLazyRescale;
+                }
+            } else {  // interior tile: every key visible to every real row (padding rows stay -inf)
+#pragma unroll
+                for (int c = 0; c < HR / 8; ++c)
+                    if (c < live_chunks) {
+#pragma unroll
+                        for (int i = 8 * c; i < 8 * c + 8; ++i) {
+                            s[i] *= p.scale_log2;
+                            need |= s[i] > m_run[i] + kLazyRescale;
+                        }
+                    }
             }
             const unsigned any = __ballot_sync(0xffffffffu, need);
             if (lane == 0) flags[8 + 16 * (t & 1) + sw] = any != 0u;
@@ -519,8 +539,7 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
                     const int r = r0 + i;
                     const float m_new =
                         fmaxf(m_run[i], fmaxf(fmaxf(red[r], red[NR + r]), fmaxf(red[2 * NR + r], red[3 * NR + r])));
-                    const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-                    alpha[i] = ex2(m_run[i] - m_use);
+                    alpha[i] = ex2(m_run[i] - m_new);
                     m_run[i] = m_new;
                     l_run[i] *= alpha[i];
                 }
@@ -555,9 +574,12 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             uint32_t hi_w[HR / 2], lo_w[HR / 2];
 #pragma unroll
             for (int i = 0; i < HR; i += 2) {
-                const float ma = m_run[i] == -CUDART_INF_F ? 0.f : m_run[i];
-                const float mb = m_run[i + 1] == -CUDART_INF_F ? 0.f : m_run[i + 1];
-                const float pa = ex2(s[i] - ma), pb = ex2(s[i + 1] - mb);
+                if (i >= 8 * live_chunks) {  // padding rows
+                    hi_w[i / 2] = 0u;
+                    lo_w[i / 2] = 0u;
+                    continue;
+                }
+                const float pa = ex2(s[i] - m_run[i]), pb = ex2(s[i + 1] - m_run[i + 1]);
                 l_run[i] += pa;
                 l_run[i + 1] += pb;
                 const __nv_bfloat162 h = __floats2bfloat162_rn(pa, pb);
