@@ -492,7 +492,11 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             const bool causal_tile = p.source != KEYS_RING && key0 + TK - 1 > qpos0;
             const bool key_tile = tags != nullptr || key0 + TK > k_end;
             const int64_t rel = qpos0 - kabs;  // key visible to row r iff rel + r / group >= 0
+            // The logit in log2 units is s * f: boundary tiles store the scaled,
+            // masked logit in s (f = 1); interior tiles keep the raw product and
+            // fold the scale into the FFMA s * f - m of the vote and of P.
             bool need = false;
+            float f = 1.f;
             if (key_tile || causal_tile) {
 #pragma unroll
                 for (int i = 0; i < HR; ++i) {
@@ -501,17 +505,15 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
                     if (causal_tile) ok = ok && rel + (r0 + i) / p.group >= 0;
                     const float v = ok ? s[i] * p.scale_log2 : -CUDART_INF_F;
                     s[i] = v;
-                    need |= v > m_run[i] + kLazyRescale;
+                    need |= v - m_run[i] > kLazyRescale;
                 }
             } else {  // interior tile: every key visible to every real row (padding rows stay -inf)
+                f = p.scale_log2;
 #pragma unroll
                 for (int c = 0; c < HR / 8; ++c)
                     if (c < live_chunks) {
 #pragma unroll
-                        for (int i = 8 * c; i < 8 * c + 8; ++i) {
-                            s[i] *= p.scale_log2;
-                            need |= s[i] > m_run[i] + kLazyRescale;
-                        }
+                        for (int i = 8 * c; i < 8 * c + 8; ++i) need |= fmaf(s[i], f, -m_run[i]) > kLazyRescale;
                     }
             }
             const unsigned any = __ballot_sync(0xffffffffu, need);
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
             if (rescale) {
 #pragma unroll
                 for (int i = 0; i < HR; ++i) {
-                    float mx = s[i];
+                    float mx = i < 8 * live_chunks ? s[i] * f : -CUDART_INF_F;
 #pragma unroll
                     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                     if (lane == 0) red[NR * q4 + r0 + i] = mx;
@@ -579,7 +581,7 @@ __global__ void __launch_bounds__(tc_threads(NR), 1)
                     lo_w[i / 2] = 0u;
                     continue;
                 }
-                const float pa = ex2(s[i] - m_run[i]), pb = ex2(s[i + 1] - m_run[i + 1]);
+                const float pa = ex2(fmaf(s[i], f, -m_run[i])), pb = ex2(fmaf(s[i + 1], f, -m_run[i + 1]));
                 l_run[i] += pa;
                 l_run[i + 1] += pb;
                 const __nv_bfloat162 h = __floats2bfloat162_rn(pa, pb);

@@ -75,6 +75,29 @@ def test_verify_shapes(D, G, T):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("scale", [-0.21, 0.0, 1e-3])
+def test_negative_zero_and_tiny_softmax_scales(D, scale):
+    """The scale is any finite float: a negative one flips which keys dominate,
+    zero gives uniform weights (lse = ln of the key count).  Verify and draft."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(150 + D)
+    B, Hkv, G, T, cap = 2, 2, 4, 3, 900
+    lens = [850, 333]
+    k, v = rand_bf16((B, Hkv, cap, D), gen, dev), rand_bf16((B, Hkv, cap, D), gen, dev)
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev)
+    kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev))
+    out, lse = wm.verify_attn(kv, q, scale)
+    ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), lens, scale)
+    assert_close(f"verify D={D} scale={scale}", out, lse, ref, ref_lse)
+    ring = wm.Ring.create(B, Hkv, D, 4, 300, dev)
+    wm.ring_fill(ring, kv)
+    qd = rand_bf16((B, Hkv * G, D), gen, dev)
+    out, lse = wm.draft_attn(ring, qd, scale)
+    ref, ref_lse = oracle.draft(oracle_kv(k, v), qd.cpu(), [n - 1 for n in lens], 4, 300, scale)
+    assert_close(f"draft D={D} scale={scale}", out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("S,W", [(0, 1), (0, 100), (4, 60), (16, 200), (3, 1)])
 def test_draft_ring_wraps(D, S, W):
     """Appends past several wraps of a small window; every step checked."""
