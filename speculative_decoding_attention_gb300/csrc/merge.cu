@@ -2,12 +2,14 @@
 //
 // Per row r with parts s = 0..n-1 (each part normalised by its own softmax sum):
 //   M = max_s lse_s,  lse = M + ln sum_s exp(lse_s - M),  o = sum_s exp(lse_s - lse) o_s.
-// A part with lse = -inf holds no key; it gets weight 0 and its o is not read.
+// A part with lse = -inf holds no key; it gets weight 0 (its o is loaded, not used).
 //
 // One CTA per (row, 32-column block).  Its 128 threads are 8 column threads
-// (one float4 each) x 16 part groups, so the loads of different parts are
-// independent and in flight together; the 16 group sums meet in shared
-// memory.  Every CTA of a row recomputes the row's lse (n_parts floats).
+// (one float4 each) x 16 part groups.  Each thread folds its parts (every
+// 16th) in one pass with a running maximum -- the part's lse and o loads do
+// not depend on each other or on earlier parts, so they are all in flight
+// together -- and the 16 group states (max, sum of weights, weighted o) meet
+// in shared memory.
 //
 // After a fused draft step the merge also commits the append: the first CTA
 // of each sequence's rows advances n_seen[b] by one.  The attention grid has
@@ -34,75 +36,81 @@ __global__ void __launch_bounds__(kMergeThreads)
     lse_merge_kernel(const float *__restrict__ o_parts, const float *__restrict__ lse_parts, int n_parts,
                      int head_dim, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out,
                      int64_t *__restrict__ commit_n_seen, int rows_per_seq) {
-    __shared__ float red[kMergeThreads / 32];
+    __shared__ float m_s[kPartGroups][kColThreads], z_s[kPartGroups][kColThreads];
     __shared__ float4 acc_s[kPartGroups][kColThreads];
     pdl_wait();
     pdl_launch_dependents();
     const int64_t r = blockIdx.x;
-    const float *ls = lse_parts + r * n_parts;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     if (commit_n_seen && blockIdx.y == 0 && tid == 0 && r % rows_per_seq == 0) {
         const int64_t b = r / rows_per_seq;
         const int64_t seen = commit_n_seen[b];
         if (seen >= 0) commit_n_seen[b] = seen + 1;  // a negative count was reported, nothing appended
     }
-
-    float mx = -CUDART_INF_F;
-    for (int s = tid; s < n_parts; s += kMergeThreads) mx = fmaxf(mx, ls[s]);
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    mx = red[0];
-#pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-    __syncthreads();
-    float z = 0.f;
-    if (mx != -CUDART_INF_F)
-        for (int s = tid; s < n_parts; s += kMergeThreads) z += ex2((ls[s] - mx) * kLog2e);
-    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane == 0) red[warp] = z;
-    __syncthreads();
-    float zt = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) zt += red[w];
-    const float lse = zt > 0.f ? mx + lg2(zt) * kLn2 : -CUDART_INF_F;
-
+    const float *ls = lse_parts + r * n_parts;
     const int ct = tid % kColThreads, pg = tid / kColThreads;
     const int col = (blockIdx.y * kColThreads + ct) * 4;
+    const bool in_cols = col < head_dim;
+    const float *op = o_parts + r * (int64_t)n_parts * head_dim + (in_cols ? col : 0);
+
+    // this group's parts, in log2 units: m = max lse, z = sum 2^(lse - m), acc = sum 2^(lse - m) o
+    float m = -CUDART_INF_F, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < head_dim && lse != -CUDART_INF_F) {
-        const float *op = o_parts + r * (int64_t)n_parts * head_dim + col;
 #pragma unroll 4
-        for (int s = pg; s < n_parts; s += kPartGroups) {
-            const float w = ex2((ls[s] - lse) * kLog2e);
-            if (w == 0.f) continue;  // empty part (lse -inf): its o is never read
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(op + (int64_t)s * head_dim));
+    for (int s = pg; s < n_parts; s += kPartGroups) {
+        const float l = __ldg(ls + s) * kLog2e;
+        const float4 v = in_cols ? __ldg(reinterpret_cast<const float4 *>(op + (int64_t)s * head_dim))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (l == -CUDART_INF_F) continue;  // an empty part: its o is not used
+        if (l > m) {
+            const float c = ex2(m - l);  // 0 while m is -inf
+            z = z * c + 1.f;
+            acc.x = acc.x * c + v.x;
+            acc.y = acc.y * c + v.y;
+            acc.z = acc.z * c + v.z;
+            acc.w = acc.w * c + v.w;
+            m = l;
+        } else {
+            const float w = ex2(l - m);
+            z += w;
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
         }
     }
+    m_s[pg][ct] = m;
+    z_s[pg][ct] = z;
     acc_s[pg][ct] = acc;
     __syncthreads();
-    if (pg == 0 && col < head_dim) {
-        float4 t = acc_s[0][ct];
+    if (pg != 0) return;
+    float mt = -CUDART_INF_F;
 #pragma unroll
-        for (int g = 1; g < kPartGroups; ++g) {
+    for (int g = 0; g < kPartGroups; ++g) mt = fmaxf(mt, m_s[g][ct]);
+    float zt = 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mt != -CUDART_INF_F) {
+#pragma unroll
+        for (int g = 0; g < kPartGroups; ++g) {
+            const float c = ex2(m_s[g][ct] - mt);  // 0 for a group without a part
             const float4 u = acc_s[g][ct];
-            t.x += u.x;
-            t.y += u.y;
-            t.z += u.z;
-            t.w += u.w;
+            zt += c * z_s[g][ct];
+            t.x += c * u.x;
+            t.y += c * u.y;
+            t.z += c * u.z;
+            t.w += c * u.w;
         }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(t.x, t.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
+    }
+    const float inv = zt > 0.f ? 1.f / zt : 0.f;
+    if (in_cols) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(t.z * inv, t.w * inv);
         uint2 pk;
         pk.x = *reinterpret_cast<const uint32_t *>(&lo);
         pk.y = *reinterpret_cast<const uint32_t *>(&hi);
         *reinterpret_cast<uint2 *>(out + r * head_dim + col) = pk;
     }
-    if (blockIdx.y == 0 && tid == 0 && lse_out) lse_out[r] = lse;
+    if (blockIdx.y == 0 && ct == 0 && lse_out) lse_out[r] = zt > 0.f ? (mt + lg2(zt)) * kLn2 : -CUDART_INF_F;
 }
 
 }  // namespace
