@@ -66,6 +66,11 @@ struct AttnCfg {
     static_assert(STAGES >= 2, "need at least double buffering");
 };
 
+// Ring tags a draft CTA stages in shared memory with Q (its whole split, when
+// it has at most this many keys; longer splits read them from global memory a
+// tile ahead).
+constexpr int kTagCache = 1024;
+
 template <int D, int MT>
 struct AttnSmem {
     static constexpr int ROWS = MT * 16;
@@ -77,7 +82,8 @@ struct AttnSmem {
     static constexpr int BAR_OFF = RED_OFF + RED_BYTES;            // full[STAGES], empty[STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + 2 * AttnCfg<D>::STAGES * 8;
     static constexpr int NEW_OFF = FLAG_OFF + 16;                  // fused step: appended K and V rows
-    static constexpr int TOTAL = NEW_OFF + 2 * D * 2 + 1024;       // + slack to 1024-align the base
+    static constexpr int TAG_OFF = NEW_OFF + 2 * D * 2;            // ring tags of the split (draft)
+    static constexpr int TOTAL = TAG_OFF + kTagCache * 4 + 1024;   // + slack to 1024-align the base
     static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && P_BYTES % 1024 == 0,
                   "swizzled regions need 1024-byte alignment");
     static_assert(NEW_OFF % 16 == 0, "16-byte vectors");
@@ -120,15 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // every global read below may depend on the previous kernel
     pdl_launch_dependents();
 
-    // ---- keys of this split, and the position of query 0
-    int64_t n_keys, qpos0;
-    int64_t new_slot = -1;  // STEP: ring slot receiving position qpos0
+    // ---- keys of this split, and the position of query 0.  The ring's key
+    // range does not depend on n_seen: only the compute warps read it (below),
+    // so the producer's first copies are not held up by that load.
+    int64_t n_keys, qpos0 = -1;
     if (p.source == KEYS_RING) {
-        int64_t seen = p.n_seen[b];
-        if (seen < 0) {
-            if (threadIdx.x == 0) report_error(p.err, WM_DEVERR_BAD_LENGTH);
-            seen = STEP ? -1 : 0;  // STEP: nothing is appended, every key is masked
-        }
         n_keys = p.n_slots;
         if (p.mem_count) {  // memory slots follow the ring's (tile-rounded) slots
             int64_t mc = p.mem_count[b];
@@ -138,8 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             n_keys = p.mem_base + mc;
         }
-        qpos0 = STEP ? seen : seen - 1;
-        if (STEP && seen >= 0) new_slot = seen < p.sink ? seen : p.sink + (seen - p.sink) % p.window;
     } else {
         int64_t len = p.seq_lens[b];
         if (len < 0 || len > p.capacity) {
@@ -226,6 +226,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // =========================================================== compute warps
     constexpr int NCT = C::NW * 32;  // compute threads
+    // Prologue: issue every load first (n_seen, the split's ring tags, Q), then
+    // store, so that their latencies overlap each other and the first tile's copy.
+    const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
+    int32_t *s_tags = reinterpret_cast<int32_t *>(gbase + L::TAG_OFF);
+    const int64_t ring_end = min(k_end, (int64_t)p.n_slots);  // memory slots carry no tag
+    const bool tags_cached = tags && ring_end - k_begin <= kTagCache;
+    constexpr int TPT = kTagCache / NCT;  // staged tags per thread
+    int64_t seen = p.source == KEYS_RING ? p.n_seen[b] : 0;
+    int32_t tag_v[TPT];
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * NCT;
+        tag_v[j] = tags_cached && i < ring_end - k_begin ? __ldg(tags + k_begin + i) : -1;
+    }
+    constexpr int VPR = D / 8;              // 16-byte vectors per row
+    constexpr int QPT = ROWS * VPR / NCT;   // Q vectors per thread
+    static_assert(ROWS * VPR % NCT == 0, "Q staging: whole vectors per thread");
+    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+    uint4 q_v[QPT];
+#pragma unroll
+    for (int j = 0; j < QPT; ++j) {
+        const int idx = threadIdx.x + j * NCT;
+        const int r = idx / VPR, v = idx - (idx / VPR) * VPR;
+        q_v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.rows) {
+            const int i = r / p.group, hh = r - i * p.group;
+            const int64_t row = ((int64_t)b * p.n_q + i) * p.n_q_heads + kvh * p.group + hh;
+            q_v[j] = __ldg(reinterpret_cast<const uint4 *>(qg + row * D) + v);
+        }
+    }
+    int64_t new_slot = -1;  // STEP: ring slot receiving position qpos0
+    if (p.source == KEYS_RING) {
+        if (seen < 0) {
+            if (threadIdx.x == 0) report_error(p.err, WM_DEVERR_BAD_LENGTH);
+            seen = STEP ? -1 : 0;  // STEP: nothing is appended, every key is masked
+        }
+        qpos0 = STEP ? seen : seen - 1;
+        if (STEP && seen >= 0) new_slot = seen < p.sink ? seen : p.sink + (seen - p.sink) % p.window;
+    }
     // STEP: the CTA whose keys include slot(p) stages the appended K row
     // (threads 0..D/8-1) and V row (D/8..D/4-1) in shared memory with Q.
     constexpr int NVR = D / 8;
@@ -235,18 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 *src = static_cast<const uint4 *>(threadIdx.x < NVR ? p.k_new : p.v_new);
         s_new[threadIdx.x] = __ldg(src + ((int64_t)b * p.n_kv_heads + kvh) * NVR + threadIdx.x % NVR);
     }
-    {
-        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-        constexpr int VPR = D / 8;  // 16-byte vectors per row
-        for (int idx = threadIdx.x; idx < ROWS * VPR; idx += NCT) {
-            const int r = idx / VPR, v = idx - (idx / VPR) * VPR;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < p.rows) {
-                const int i = r / p.group, hh = r - i * p.group;
-                const int64_t row = ((int64_t)b * p.n_q + i) * p.n_q_heads + kvh * p.group + hh;
-                val = __ldg(reinterpret_cast<const uint4 *>(q + row * D) + v);
-            }
-            st_shared_v4(sQ + (v >> 3) * (ROWS * 128) + swz128(r, v & 7), val);
+#pragma unroll
+    for (int j = 0; j < QPT; ++j) {
+        const int idx = threadIdx.x + j * NCT;
+        const int r = idx / VPR, v = idx - (idx / VPR) * VPR;
+        st_shared_v4(sQ + (v >> 3) * (ROWS * 128) + swz128(r, v & 7), q_v[j]);
+    }
+    if (tags_cached) {
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * NCT;
+            if (i < ring_end - k_begin) s_tags[i] = tag_v[j];
         }
     }
     named_bar_sync(1, NCT);
@@ -275,20 +313,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[m][n][e] = 0.f;
     }
-    const int32_t *tags = p.source == KEYS_RING ? p.pos_tag + (int64_t)b * p.n_slots : nullptr;
     // Ring slot tags this thread needs for one tile: the four keys of its S
-    // fragment and (lanes < 16) the key it checks for V-row zeroing.  They are
-    // fetched one tile ahead so that their latency hides behind the tile.
+    // fragment and (lanes < 16) the key it checks for V-row zeroing.  Read from
+    // the staged copy when the split fits it; otherwise fetched from global
+    // memory one tile ahead so that their latency hides behind the tile.
+    const bool tags_global = tags && !tags_cached;
     auto fetch_tags = [&](int64_t key0, int32_t(&tg)[2][2], int32_t &tg1) {
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
-                tg[n][e] = (tags && kabs < k_end && kabs < p.n_slots) ? __ldg(tags + kabs) : -1;
+                tg[n][e] = kabs < ring_end ? __ldg(tags + kabs) : -1;
             }
         const int64_t kl = key0 + warp * C::KPW + lane;
-        tg1 = (tags && lane < C::KPW && kl < k_end && kl < p.n_slots) ? __ldg(tags + kl) : -1;
+        tg1 = (lane < C::KPW && kl < ring_end) ? __ldg(tags + kl) : -1;
+    };
+    auto tag_of_key = [&](int64_t kabs, int32_t prefetched) -> int32_t {
+        if (!tags_cached) return prefetched;
+        return kabs < ring_end ? s_tags[kabs - k_begin] : -1;
     };
     auto tag_ok = [&](int64_t tg) {
         return tg >= 0 && tg <= qpos0 && (tg < p.sink || tg > qpos0 - p.window);
@@ -297,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tag_of = [&](int64_t kabs, int32_t tg) -> int64_t {
         return STEP && kabs == new_slot ? qpos0 : (int64_t)tg;
     };
-    int32_t tg_cur[2][2], tg1_cur, tg_nxt[2][2], tg1_nxt;
-    if (tags && n_tiles > 0) fetch_tags(k_begin, tg_cur, tg1_cur);
+    int32_t tg_cur[2][2] = {{-1, -1}, {-1, -1}}, tg1_cur = -1, tg_nxt[2][2], tg1_nxt;
+    if (tags_global && n_tiles > 0) fetch_tags(k_begin, tg_cur, tg1_cur);
 
     for (int t = 0; t < n_tiles; ++t) {
-        if (tags && t + 1 < n_tiles) fetch_tags(k_begin + (int64_t)(t + 1) * TK, tg_nxt, tg1_nxt);
+        if (tags_global && t + 1 < n_tiles) fetch_tags(k_begin + (int64_t)(t + 1) * TK, tg_nxt, tg1_nxt);
         const int s = t % C::STAGES;
         const int buf = t & 1;
         if (!*abort_flag && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, kWaitLimit)) {
@@ -364,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
                 const int64_t kabs = key0 + warp * C::KPW + n * 8 + 2 * t4 + e;
                 bool ok = kabs < k_end;
-                if (ok && tags) ok = kabs >= mem_lo || tag_ok(tag_of(kabs, tg_cur[n][e]));
+                if (ok && tags) ok = kabs >= mem_lo || tag_ok(tag_of(kabs, tag_of_key(kabs, tg_cur[n][e])));
                 key_ok[n][e] = ok;
             }
 #pragma unroll
@@ -396,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < C::KPW) {
                 const int64_t kabs = key0 + warp * C::KPW + lane;
                 ok_all = kabs < k_end;
-                if (ok_all && tags) ok_all = kabs >= mem_lo || tag_ok(tag_of(kabs, tg1_cur));
+                if (ok_all && tags) ok_all = kabs >= mem_lo || tag_ok(tag_of(kabs, tag_of_key(kabs, tg1_cur)));
             }
             uint32_t bad = ~__ballot_sync(0xffffffffu, ok_all) & ((1u << C::KPW) - 1u);
             if (bad) {
@@ -494,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (tags) {
+        if (tags_global) {
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
