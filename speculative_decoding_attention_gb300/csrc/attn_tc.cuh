@@ -81,16 +81,25 @@ struct TcLayout {
     static constexpr bool FITS = TOTAL <= 227 * 1024;
 };
 
+// Two CTAs per SM for 16-row tiles at head_dim 128: a 16-row tile has too
+// little softmax work to hide its per-tile hand-off chain, and a second CTA's
+// independent chain does (the ragged paged verify went from 56% to 87% of
+// HBM).  Two 32 KB slots each, so both fit in shared memory.
+__host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 128 && nr == 16; }
+
 // Shared-memory plan: the most K/V staging slots (up to 6) that fit with one
 // P^T buffer -- keeping enough HBM requests in flight per SM (well over 100 KB
 // at loaded HBM latency) matters most -- then a second P^T buffer if it fits.
 template <int D, int NR>
 struct TcPlan {
-    static constexpr int NSLOT = TcLayout<D, NR, 6, 1>::FITS   ? 6
+    static constexpr int NSLOT = tc_two_per_sm(D, NR)            ? 2
+                                 : TcLayout<D, NR, 6, 1>::FITS   ? 6
                                  : TcLayout<D, NR, 5, 1>::FITS ? 5
                                  : TcLayout<D, NR, 4, 1>::FITS ? 4
                                  : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
-    static constexpr int NPB = TcLayout<D, NR, NSLOT, 2>::FITS ? 2 : 1;
+    static constexpr int NPB = !tc_two_per_sm(D, NR) && TcLayout<D, NR, NSLOT, 2>::FITS ? 2 : 1;
+    static_assert(!tc_two_per_sm(D, NR) || 2 * TcLayout<D, NR, NSLOT, NPB>::TOTAL <= 228 * 1024,
+                  "two CTAs per SM must fit in shared memory");
 };
 
 template <int D, int NR>
@@ -133,7 +142,7 @@ __device__ __forceinline__ bool in_smem(uint32_t lo, uint32_t len, uint32_t base
 }
 
 template <int D, int NR>
-__global__ void __launch_bounds__(tc_threads(NR), 1)
+__global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const AttnParams p) {
     using C = TcCfg<D, NR>;
@@ -731,6 +740,23 @@ cudaError_t launch_attn_tc_nr(const CUtensorMap &k, const CUtensorMap &v, const 
     return launch_pdl(attn_tc_kernel<D, NR>, grid, dim3(TcCfg<D, NR>::THREADS), smem, stream, k, v, p);
 }
 
+template <int D, int NR>
+int tc_blocks_per_sm_nr() {
+    constexpr int smem = TcCfg<D, NR>::TOTAL;
+    if (cudaFuncSetAttribute(attn_tc_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_tc_kernel<D, NR>, TcCfg<D, NR>::THREADS, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 template <int D>
 cudaError_t launch_attn_tc(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int n_rows16,
                            cudaStream_t stream) {
@@ -740,6 +766,17 @@ cudaError_t launch_attn_tc(const CUtensorMap &k, const CUtensorMap &v, const Att
         case 48: return launch_attn_tc_nr<D, 48>(k, v, p, stream);
         case 64: return launch_attn_tc_nr<D, 64>(k, v, p, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D>
+int tc_blocks_per_sm(int n_rows16) {
+    switch (n_rows16) {
+        case 16: return tc_blocks_per_sm_nr<D, 16>();
+        case 32: return tc_blocks_per_sm_nr<D, 32>();
+        case 48: return tc_blocks_per_sm_nr<D, 48>();
+        case 64: return tc_blocks_per_sm_nr<D, 64>();
+        default: return 0;
     }
 }
 

@@ -8,4 +8,6 @@ cudaError_t launch_attn_tc_d128(const CUtensorMap &k, const CUtensorMap &v, cons
     return launch_attn_tc<128>(k, v, p, n_rows16, stream);
 }
 
+int attn_tc_blocks_per_sm_d128(int n_rows16) { return tc_blocks_per_sm<128>(n_rows16); }
+
 }  // namespace wm

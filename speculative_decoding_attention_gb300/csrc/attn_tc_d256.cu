@@ -8,4 +8,6 @@ cudaError_t launch_attn_tc_d256(const CUtensorMap &k, const CUtensorMap &v, cons
     return launch_attn_tc<256>(k, v, p, n_rows16, stream);
 }
 
+int attn_tc_blocks_per_sm_d256(int n_rows16) { return tc_blocks_per_sm<256>(n_rows16); }
+
 }  // namespace wm

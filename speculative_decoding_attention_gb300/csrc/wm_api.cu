@@ -96,11 +96,10 @@ int key_tile(int op, int head_dim) { return use_tc_kernel(op, head_dim) ? kTcTil
 // K+V bytes per split when a batch may be ragged (see plan_splits).
 constexpr int64_t kRaggedSplitBytes = 8ll << 20;
 
-// Resident CTAs per SM of the kernel that serves `op` (the tcgen05 verify
-// kernel: one).  For the draft the smaller of the plain and the fused-step
-// instances, so that both split alike.  At least 1 (also without a device).
+// Resident CTAs per SM of the kernel that serves `op`.  For the draft the
+// smaller of the plain and the fused-step instances, so that both split alike.
+// At least 1 (also without a device).
 int ctas_per_sm(int op, int head_dim, int rows) {
-    if (use_tc_kernel(op, head_dim)) return 1;
     static std::mutex mu;
     static int cache[kMaxDevices][3][4][2] = {};
     int dev = 0;
@@ -110,7 +109,9 @@ int ctas_per_sm(int op, int head_dim, int rows) {
     const int oi = op == WM_OP_VERIFY ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
     int &n = cache[dev][di][mt - 1][oi];
-    if (!n) {
+    if (!n && use_tc_kernel(op, head_dim)) {
+        n = std::max(1, head_dim == 128 ? attn_tc_blocks_per_sm_d128(16 * mt) : attn_tc_blocks_per_sm_d256(16 * mt));
+    } else if (!n) {
         auto query = [&](bool step) {
             return di == 0 ? attn_blocks_per_sm_d64(mt, step)
                  : di == 1 ? attn_blocks_per_sm_d128(mt, step) : attn_blocks_per_sm_d256(mt, step);

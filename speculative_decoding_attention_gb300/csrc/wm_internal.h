@@ -106,6 +106,9 @@ cudaError_t launch_attn_tc_d128(const CUtensorMap &k, const CUtensorMap &v, cons
 cudaError_t launch_attn_tc_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p,
                                 int n_rows16, cudaStream_t stream);
 constexpr int kTcTile = 128;
+// Resident CTAs per SM of the tcgen05 kernel for n_rows16 rows (0 if unknown).
+int attn_tc_blocks_per_sm_d128(int n_rows16);
+int attn_tc_blocks_per_sm_d256(int n_rows16);
 
 // Ring and merge kernels (ring.cu, merge.cu).
 cudaError_t launch_ring_append(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,
