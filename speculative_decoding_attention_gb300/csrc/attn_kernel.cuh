@@ -33,10 +33,15 @@
 // new count early.  Same splits and merge as the unfused draft, so the outputs
 // are bit-identical to ring append + draft attention.
 //
+// Memory slots (memory-augmented draft): keys at or beyond mem_base are the
+// materialized slots 0..count[b]-1 of a second store, read through the second
+// pair of tensor maps, and every row sees all of them.
+//
 // Masks: verification is causal (query i sees positions <= seq_len - n_q + i);
 // the draft sees a ring slot iff its tag t satisfies 0 <= t <= p and
-// (t < sink or t > p - window).  Keys masked for every row get their V row
-// zeroed in shared memory so that stale or uninitialised cache bytes (even NaN
+// (t < sink or t > p - window); the split's tags are staged in shared memory
+// with Q when they fit.  Keys masked for every row get their V row zeroed in
+// shared memory so that stale or uninitialised cache bytes (even NaN
 // patterns) cannot reach the output through 0 * NaN.
 #pragma once
 

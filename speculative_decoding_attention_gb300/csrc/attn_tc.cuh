@@ -12,7 +12,9 @@
 // kept per key-thread in registers and reduced once at the end.  The shared
 // memory split between K/V staging slots and P^T buffers is chosen per head
 // dim and row count: as many staging slots as fit, then a second P^T buffer
-// if it still fits.  Warp roles (2 + 4g warps, g = NR / 8 up to 32 rows, else NR / 16):
+// if it still fits -- except 16-row tiles at head_dim 128, which take two
+// slots so that two CTAs share an SM.  Warp roles (2 + 4g warps, g = NR / 8
+// up to 32 rows, else NR / 16):
 //   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
 //               shared-memory slots, K_t then V_t;
 //   warp 1    : allocates tensor memory; one lane issues whichever MMA is ready
@@ -20,9 +22,10 @@
 //               written) and commits it to mbarriers;
 //   warps 2.. : softmax -- one key per thread (a tensor-memory lane), g warps
 //               per lane quadrant each owning NR / g rows: scale and mask
-//               the logits, keep a running row maximum that is raised (with a
-//               rescale of O and L) only when a logit exceeds it by more than
-//               2^8, write P^T to shared memory as two bf16 parts
+//               the logits, keep a running row maximum (from a finite floor)
+//               that is raised (with a rescale of O and L) only when a logit
+//               exceeds it by more than 2^8, write P^T to shared memory as two
+//               bf16 parts
 //               (hi = bf16(p), lo = bf16(p - hi)), and finally normalise and
 //               store the output.  P^T is double-buffered when shared memory
 //               allows, so the softmax of tile t+1 overlaps P_t.V_t.
