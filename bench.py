@@ -1,11 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of one Windowed-MTP speculative-decoding attention step on GB300.
 
-A step is the whole hot path over one batch: d draft steps (ring append +
-sink/window draft attention, each with its split merge) and the verification
-attention of T = d + 1 positions over the full bf16 KV cache (+ merge), then a
-rollback of the d speculative ring entries so every timed step sees the same
-state.  It runs as one CUDA graph; the L2 is flushed between timed steps.
+A step is the whole hot path over one batch: d draft steps (each the fused
+ring append + sink/window draft attention, then its split merge) and the
+verification attention of T = d + 1 positions over the full bf16 KV cache
+(+ merge), then a rollback of the d speculative ring entries so every timed
+step sees the same state.  It runs as one CUDA graph; the L2 is flushed between
+timed steps.  Defaults: 10 warm-up and 50 timed steps.
 
 Default workload: 1M-token context, full-attention layer of a hybrid target
 (GQA 8, head_dim 256, S=4, W=4096), draft depth 3.
@@ -45,8 +46,8 @@ KERNEL_SOURCES = ("attn_tc.cuh", "tc.cuh", "ptx.cuh", "wm_internal.h")
 def parse():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default=workloads.BENCH_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--depth", type=int, default=None, help="draft depth d (verify T = d + 1)")
@@ -379,6 +380,7 @@ def gpu_arm(args, rank, world, local):
             "execution": "one CUDA graph per step", "parallelism": f"replicas x{world}",
         },
         "detail": {
+            "step_us_median": round(1e3 * sorted(step_ms)[len(step_ms) // 2], 2),
             "verify_us": round(us_verify, 2),
             "verify_gbs": round(achieved, 1),
             "draft_chain_us": None if us_draft is None else round(us_draft, 2),
