@@ -122,3 +122,55 @@ def test_memory_count_beyond_capacity_is_clamped_and_reported():
     torch.cuda.synchronize()
     assert wm.get_device_error() == 1
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)) and torch.equal(lse, ref_lse)
+
+
+def test_memory_rollback_then_draft_sees_the_kept_slots():
+    """After a rejection the slots materialized past the accepted prefix are
+    discarded: the draft attends to slots 0..new_count-1 only."""
+    B, Hkv, G, D, S, W, lens, cap = 2, 2, 4, 128, 4, 128, [700, 300], 12
+    dev, gen, hk, hv, ring, mk, mv, mem = build(B, Hkv, D, S, W, lens, cap, [12, 9], seed=61)
+    wm.mem_rollback(mem, torch.tensor([5, 9], device=dev))
+    assert mem.count.tolist() == [5, 9]
+    q = rand_bf16((B, Hkv * G, D), gen, dev)
+    out, lse = wm.draft_attn_mem(ring, mem, q, D ** -0.5)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.draft_mem(oracle_kv(hk, hv), oracle_kv(mk, mv), [5, 9], q.cpu(), [n - 1 for n in lens],
+                                    S, W, D ** -0.5)
+    assert_close("after memory rollback", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
+def test_fused_step_with_memory_in_a_graph():
+    """A captured fused step with memory, replayed: each replay appends the next
+    position to the ring, a slot is materialized between replays."""
+    B, Hkv, G, D, S, W, lens, cap, steps = 1, 2, 8, 128, 4, 256, [1500], 8, 4
+    dev, gen, hk, hv, ring, mk, mv, mem = build(B, Hkv, D, S, W, lens, cap, [2], seed=62, extra=steps)
+    ws = wm.step_workspace(ring, Hkv * G, mem=mem)
+    kn = torch.stack([hk[b, :, n] for b, n in enumerate(lens)]).contiguous()
+    vn = torch.stack([hv[b, :, n] for b, n in enumerate(lens)]).contiguous()
+    q = rand_bf16((B, Hkv * G, D), gen, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hkv * G), dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        wm.draft_step(ring, kn, vn, q, D ** -0.5, ws, out=out, lse=lse, stream=side, mem=mem)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    hist, mhist = oracle_kv(hk, hv), oracle_kv(mk, mv)
+    ref, ref_lse = oracle.draft_mem(hist, mhist, [2], q.cpu(), [lens[0]], S, W, D ** -0.5)
+    assert_close("eager", out, lse, ref, ref_lse)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        wm.draft_step(ring, kn, vn, q, D ** -0.5, ws, out=out, lse=lse, stream=torch.cuda.current_stream(), mem=mem)
+    for j in range(1, steps):
+        wm.mem_append(mem, mk[:, :, 1 + j].contiguous(), mv[:, :, 1 + j].contiguous())
+        kn.copy_(torch.stack([hk[b, :, n + j] for b, n in enumerate(lens)]))
+        vn.copy_(torch.stack([hv[b, :, n + j] for b, n in enumerate(lens)]))
+        q.copy_(rand_bf16((B, Hkv * G, D), gen, dev))
+        g.replay()
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle.draft_mem(hist, mhist, [2 + j], q.cpu(), [lens[0] + j], S, W, D ** -0.5)
+        assert_close(f"replay {j}", out, lse, ref, ref_lse)
+    assert ring.n_seen.tolist() == [lens[0] + steps] and mem.count.tolist() == [2 + steps - 1]
+    assert wm.get_device_error() == 0
