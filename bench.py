@@ -105,9 +105,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, depth: int):
+def profiled_traffic(workload: str, depth: int, context=None):
     """DRAM bytes per verify launch from the committed ncu summary, if it was
-    taken on the current kernel source for this workload; else None."""
+    taken on the current kernel source for this workload (at its own context);
+    else None."""
+    if context is not None:
+        return None
     try:
         rec = json.load(open(PROFILE_TRAFFIC))
     except (OSError, ValueError):
@@ -409,7 +412,7 @@ def gpu_arm(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peak_src} hbm_gbs",
-            "traffic": profiled_traffic(w.name, depth),
+            "traffic": profiled_traffic(w.name, depth, args.context),
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
