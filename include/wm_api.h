@@ -38,7 +38,8 @@
  *     log-sum-exp of the scaled logits in fp32.  A row with no key to attend
  *     to gets out = 0 and lse = -inf.
  *   - head_dim must be 64, 128 or 256; n_q_heads a multiple of n_kv_heads;
- *     G * (query positions) at most 64 rows per KV head.
+ *     G * (query positions) at most 64 rows per KV head; batch * n_kv_heads
+ *     at most 65535 for the attention calls (WM_ERR_UNSUPPORTED otherwise).
  */
 #ifndef WM_API_H
 #define WM_API_H

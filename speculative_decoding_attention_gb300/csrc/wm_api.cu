@@ -18,6 +18,7 @@ __device__ int32_t g_device_error;  // first device-side data error (WM_DEVERR_*
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRows = 64;  // query rows per KV head (4 m-tiles of 16)
+constexpr int64_t kMaxUnits = 65535;  // (sequence, KV head) pairs: the launch grid's y extent
 
 int32_t *device_error_ptr() {
     static int32_t *ptrs[kMaxDevices] = {};
@@ -339,6 +340,7 @@ static wm_status run_attention(int op, AttnParams &p, const MapEncoder &encode_m
                                int32_t n_split, void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
                                int64_t *commit_n_seen = nullptr) {
     const bool step = commit_n_seen != nullptr;
+    if ((int64_t)p.batch * p.n_kv_heads > kMaxUnits) return WM_ERR_UNSUPPORTED;
     const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim),
                                      p.head_dim, ctas_per_sm(op, p.head_dim, p.rows));
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;

@@ -171,6 +171,17 @@ def test_memory_draft_plans_over_ring_tiles_plus_capacity(lib):
     assert wm.plan_splits(wm.WM_OP_DRAFT_MEM, 1, 2, 16, 1, 256, 4460, 1000) == 70  # 65 + 5 tiles
 
 
+def test_too_many_sequence_head_pairs_are_unsupported(lib):
+    # 65536 (sequence, KV head) pairs exceed the launch grid: refused on the host
+    P = ctypes.c_void_p
+    r = _ring(batch=32768, n_kv_heads=2)
+    assert lib.wm_draft_attn(ctypes.byref(r), P(1 << 24), 8, 1.0, 4, P(1 << 25), None, P(1 << 26), 1 << 40,
+                             None) == wm.WM_ERR_UNSUPPORTED
+    s = _kv(batch=65536, n_kv_heads=1)
+    assert lib.wm_verify_attn(ctypes.byref(s), P(1 << 24), 2, 8, 1.0, 4, P(1 << 25), None, P(1 << 26), 1 << 40,
+                              None) == wm.WM_ERR_UNSUPPORTED
+
+
 def test_draft_step_workspace(lib):
     # split partials (o then lse) even when unsplit: the merge commits n_seen
     for ns in (1, 4, 5):  # split counts the 65 tiles of 4100 slots divide into exactly
