@@ -39,7 +39,8 @@
  *     to gets out = 0 and lse = -inf.
  *   - head_dim must be 64, 128 or 256; n_q_heads a multiple of n_kv_heads;
  *     G * (query positions) at most 64 rows per KV head; batch * n_kv_heads
- *     at most 65535 for the attention calls (WM_ERR_UNSUPPORTED otherwise).
+ *     at most 65535 for the attention calls and wm_ring_fill, batch at most
+ *     65535 for wm_ring_rollback (WM_ERR_UNSUPPORTED otherwise).
  */
 #ifndef WM_API_H
 #define WM_API_H

@@ -293,6 +293,7 @@ wm_status wm_ring_fill(const wm_ring *ring, const wm_kv *hist, void *stream) {
     if (ks != WM_OK) return ks;
     if (hist->batch != ring->batch || hist->n_kv_heads != ring->n_kv_heads || hist->head_dim != ring->head_dim)
         return WM_ERR_INVALID_ARG;
+    if ((int64_t)ring->batch * ring->n_kv_heads > kMaxUnits) return WM_ERR_UNSUPPORTED;
     int32_t *err = device_error_ptr();
     if (!err) return WM_ERR_CUDA;
     HistSource h;
@@ -311,6 +312,7 @@ wm_status wm_ring_fill(const wm_ring *ring, const wm_kv *hist, void *stream) {
 
 wm_status wm_ring_rollback(const wm_ring *ring, const int64_t *new_len, void *stream) {
     if (!ring_ok(ring) || !new_len || !aligned(new_len, 8)) return WM_ERR_INVALID_ARG;
+    if (ring->batch > kMaxUnits) return WM_ERR_UNSUPPORTED;
     int32_t *err = device_error_ptr();
     if (!err) return WM_ERR_CUDA;
     return launch_status(launch_ring_rollback(ring->pos_tag, ring->n_seen, ring->batch,
