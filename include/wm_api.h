@@ -94,7 +94,8 @@ typedef struct wm_ring {
 
 /*
  * Compressed memory slots of a memory-augmented sliding-window draft
- * ("Memory-Augmented Sliding-Window Drafting", 4.1-4.3): at every r-token
+ * ("Strong Drafts Need Compact Memories: Long-Context Speculative Decoding
+ * with Compressed KV Cache", 4.1-4.3): at every r-token
  * boundary the draft's adaptor materializes one memory slot (its K/V come
  * from the caller; the adaptor is not part of this library) that stays after
  * the raw tokens leave the window.  A draft query attends to the sinks, the
@@ -185,9 +186,10 @@ wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, f
                         size_t workspace_bytes, void *stream);
 
 /*
- * Memory-augmented draft attention ("Memory-Augmented Sliding-Window
- * Drafting", 4.1 and Appendix C: a raw-token query sees the sink tokens, the
- * available memory slots and a bounded local window).  As wm_draft_attn, and
+ * Memory-augmented draft attention ("Strong Drafts Need Compact Memories:
+ * Long-Context Speculative Decoding with Compressed KV Cache", 4.1 and
+ * Appendix C: a raw-token query sees the sink tokens, the available memory
+ * slots and a bounded local window).  As wm_draft_attn, and
  * in the same softmax the query also attends to memory slots
  * 0 .. mem->count[b]-1.  mem must match the ring's batch, n_kv_heads and
  * head_dim.  A count outside 0..capacity records WM_DEVERR_BAD_LENGTH and is
@@ -207,7 +209,8 @@ wm_status wm_draft_attn_mem(const wm_ring *ring, const wm_mem *mem, const void *
 wm_status wm_mem_append(const wm_mem *mem, const void *k_new, const void *v_new, void *stream);
 
 /*
- * Rollback of memory slots materialized after the accepted prefix (4.3):
+ * Rollback of memory slots materialized after the accepted prefix (same
+ * page, 4.3):
  * count[b] = min(count[b], new_count[b]), new_count a device int64 [batch].
  */
 wm_status wm_mem_rollback(const wm_mem *mem, const int64_t *new_count, void *stream);

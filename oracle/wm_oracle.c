@@ -26,8 +26,9 @@
  * no running rescale.  Rows are independent; OpenMP only spreads whole rows
  * over the host cores and changes no arithmetic.
  *
- *   - Memory-augmented draft ("Memory-Augmented Sliding-Window Drafting", 4.1
- *     and Appendix C).  The draft's working memory is the sinks, the exact
+ *   - Memory-augmented draft ("Strong Drafts Need Compact Memories:
+ *     Long-Context Speculative Decoding with Compressed KV Cache", 4.1 and
+ *     Appendix C).  The draft's working memory is the sinks, the exact
  *     local window and the compressed memory slots materialized so far; a
  *     raw-token query attends to all three, M(p) plus slots 0..count-1.
  *
@@ -277,8 +278,9 @@ int wmo_draft(const wmo_kv *hist, int n_q_heads, const uint16_t *q, const int64_
     return err;
 }
 
-/* Memory-augmented sliding-window draft ("Memory-Augmented Sliding-Window
- * Drafting", 4.1 and Appendix C): the working memory of the draft is the
+/* Memory-augmented sliding-window draft ("Strong Drafts Need Compact
+ * Memories: Long-Context Speculative Decoding with Compressed KV Cache", 4.1
+ * and Appendix C): the working memory of the draft is the
  * union of the attention sinks, the exact local window and the compressed
  * memory slots materialized so far, and an ordinary raw-token query sees
  * exactly those.  So for a query at position p of sequence b the key set is

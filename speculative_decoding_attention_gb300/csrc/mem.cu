@@ -1,5 +1,6 @@
 // mem.cu -- the memory-slot store of a memory-augmented sliding-window draft
-// ("Memory-Augmented Sliding-Window Drafting", 4.2-4.3): at every r-token
+// ("Strong Drafts Need Compact Memories: Long-Context Speculative Decoding
+// with Compressed KV Cache", 4.2-4.3): at every r-token
 // boundary the draft's adaptor materializes one compressed memory slot, which
 // stays after the raw tokens it summarizes leave the window; on rejection the
 // slots materialized after the accepted prefix are discarded.

@@ -9,9 +9,10 @@ deliberate mistake at a time and checks that some pin fails for each.
 
 Pages: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at Million-Token
 Context" (Abstract) -- draft attention over a sliding window plus attention
-sinks, full-attention verification intact; "Memory-Augmented Sliding-Window
-Drafting" (4.1, Appendix C) -- the draft's working memory adds compressed
-memory slots to the sinks and the window.
+sinks, full-attention verification intact; "Strong Drafts Need Compact
+Memories: Long-Context Speculative Decoding with Compressed KV Cache" (4.1,
+Appendix C) -- the draft's working memory adds compressed memory slots to the
+sinks and the window.
 """
 import math
 
