@@ -212,6 +212,31 @@ def test_paged_verify_matches_contiguous_oracle():
         assert_close(f"paged ns={ns}", out, lse, ref, ref_lse)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("page", [64, 128, 256])
+def test_paged_page_sizes_and_short_sequences(D, page):
+    """Paged verify over a permuted page pool at several page sizes (128-key
+    boxes when the page holds whole 128-key tiles), with an empty sequence and
+    one shorter than the verify window (its early queries see no key)."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(400 + D + page)
+    B, Hkv, G, T = 4, 2, 4, 3
+    lens = [0, 2, 70, 3 * page + 17]
+    max_pages = (max(lens) + page - 1) // page + 1
+    n_pages = B * max_pages + 3
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(7 + page))
+    block_table = perm[: B * max_pages].view(B, max_pages).to(torch.int32).to(dev)
+    k = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+    v = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev)
+    kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), block_table)
+    for ns in (0, 1, 3):
+        out, lse = wm.verify_attn(kv, q, D ** -0.5, n_split=ns)
+        ref, ref_lse = oracle.verify(oracle_kv(k, v, block_table), q.cpu(), lens, D ** -0.5)
+        assert_close(f"paged D={D} page={page} ns={ns}", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
 def test_lse_merge_kernel_matches_oracle():
     dev = gpu()
     gen = torch.Generator(device=dev).manual_seed(304)

@@ -70,6 +70,8 @@ CASES = [
     (2, 2, 4, 256, 4, 400, [700, 10], 3, 6),             # ragged last split
     (2, 2, 4, 128, 4, 1020, [3000, 1500], 3, 16),
     (1, 2, 8, 128, 4, 200, [500], 2, 100),               # more splits requested than tiles
+    (1, 2, 8, 128, 4, 2000, [5000], 2, 1),               # a split longer than the staged tags
+    (2, 2, 4, 256, 4, 3000, [3500, 900], 2, 2),          # the same at head_dim 256, two splits
 ]
 
 
