@@ -237,6 +237,38 @@ def test_paged_page_sizes_and_short_sequences(D, page):
     assert wm.get_device_error() == 0
 
 
+@pytest.mark.parametrize("G,T", [(8, 6), (16, 3), (8, 5), (16, 4), (8, 7)])
+@pytest.mark.parametrize("page", [0, 64, 256])
+def test_verify_head_dim_256_many_rows(G, T, page):
+    """head_dim 256 with 33-64 rows per KV head (the largest tensor-core row
+    tiles, where only two K/V staging slots fit): a split of ~10 tiles cycles
+    the slots many times; one and several splits, contiguous and paged, with
+    ragged ends whose masked keys have their V rows zeroed."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(500 + 3 * G + T + page)
+    B, Hkv, D = 2, 2, 256
+    lens = [1290, 5 + T // 2]
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev)
+    if page:
+        max_pages = (max(lens) + page - 1) // page + 1
+        n_pages = B * max_pages + 2
+        perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(11 + page))
+        block_table = perm[: B * max_pages].view(B, max_pages).to(torch.int32).to(dev)
+        k = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+        v = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+    else:
+        block_table = None
+        k = rand_bf16((B, Hkv, 1400, D), gen, dev)
+        v = rand_bf16((B, Hkv, 1400, D), gen, dev)
+    kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), block_table)
+    hist = oracle_kv(k, v, block_table)
+    ref, ref_lse = oracle.verify(hist, q.cpu(), lens, D ** -0.5)
+    for ns in (0, 1, 4):
+        out, lse = wm.verify_attn(kv, q, D ** -0.5, n_split=ns)
+        assert_close(f"verify D=256 G={G} T={T} page={page} ns={ns}", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
 def test_lse_merge_kernel_matches_oracle():
     dev = gpu()
     gen = torch.Generator(device=dev).manual_seed(304)
