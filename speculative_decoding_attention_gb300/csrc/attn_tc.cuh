@@ -67,8 +67,8 @@ struct TcLayout {
     static constexpr int NOC = D / 128;                        // O accumulators (M = 128 each)
     static constexpr int REGION = TK * 128;                    // one 64-column chunk of a tile
     static constexpr int SLOT_BYTES = TK * D * 2;              // one K or V tile
-    static constexpr int PT_ROW = NR <= 32 ? 64 : 128;         // bytes per key row of P^T
-    static constexpr int PT_SWIZZLE = NR <= 32 ? 4 : 2;        // 64B / 128B swizzle (descriptor code)
+    static constexpr int PT_ROW = NR <= 16 ? 32 : NR <= 32 ? 64 : 128;  // bytes per key row of P^T
+    static constexpr int PT_SWIZZLE = NR <= 16 ? 6 : NR <= 32 ? 4 : 2;  // 32B / 64B / 128B swizzle (descriptor code)
     static constexpr int PT_ATOM = PT_ROW * 8;                 // one 8-key swizzle atom
     static constexpr int Q_OFF = NSLOT * SLOT_BYTES;
     static constexpr int Q_REGION = NR * 128;
@@ -87,7 +87,7 @@ struct TcLayout {
 // Two CTAs per SM for 16-row tiles at head_dim 128: a 16-row tile has too
 // little softmax work to hide its per-tile hand-off chain, and a second CTA's
 // independent chain does (the ragged paged verify went from 56% to 87% of
-// HBM).  Two 32 KB slots each, so both fit in shared memory.
+// HBM).  Each takes as many 32 KB slots as let both fit in shared memory.
 __host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 128 && nr == 16; }
 
 // Shared-memory plan: the most K/V staging slots (up to 6) that fit with one
@@ -95,7 +95,7 @@ __host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 12
 // at loaded HBM latency) matters most -- then a second P^T buffer if it fits.
 template <int D, int NR>
 struct TcPlan {
-    static constexpr int NSLOT = tc_two_per_sm(D, NR)            ? 2
+    static constexpr int NSLOT = tc_two_per_sm(D, NR) ? (2 * TcLayout<D, NR, 3, 1>::TOTAL <= 226 * 1024 ? 3 : 2)
                                  : TcLayout<D, NR, 6, 1>::FITS   ? 6
                                  : TcLayout<D, NR, 5, 1>::FITS ? 5
                                  : TcLayout<D, NR, 4, 1>::FITS ? 4
@@ -611,11 +611,12 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
 #pragma unroll
             for (int j = 0; j < HR / 8; ++j) {
                 // MN-major P^T: key kt's row of PT_ROW bytes, 16-byte chunks of
-                // 8 rows permuted by the 128B (chunk ^ kt%8) or 64B
-                // (chunk ^ (kt/2)%4) swizzle
+                // 8 rows permuted by the 128B (chunk ^ kt%8), 64B
+                // (chunk ^ (kt/2)%4) or 32B (chunk ^ (kt/4)%2) swizzle
                 const int chunk = r0 / 8 + j;
                 const uint32_t phys = C::PT_ROW == 128 ? (uint32_t)(chunk ^ (kt & 7))
-                                                       : (uint32_t)(chunk ^ ((kt >> 1) & 3));
+                                      : C::PT_ROW == 64 ? (uint32_t)(chunk ^ ((kt >> 1) & 3))
+                                                        : (uint32_t)(chunk ^ ((kt >> 2) & 1));
                 const uint32_t off = (uint32_t)kt * C::PT_ROW + (phys << 4);
                 st_shared_v4(pt + off, make_uint4(hi_w[4 * j], hi_w[4 * j + 1], hi_w[4 * j + 2], hi_w[4 * j + 3]));
                 st_shared_v4(pt + C::PT_BYTES + off,

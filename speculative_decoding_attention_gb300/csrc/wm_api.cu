@@ -129,17 +129,26 @@ int ctas_per_sm(int op, int head_dim, int rows) {
 // With several sequences the lengths may differ (only their maximum is known
 // on the host), so splits are also capped at about kRaggedSplitBytes of K+V:
 // short sequences then leave most of their splits empty (those CTAs exit at
-// once) and the block scheduler balances the rest.
+// once) and the block scheduler balances the rest.  When the cap asks for
+// more than one wave, the count is raised to fill the last wave (the most
+// splits that still take that many waves): with equal lengths a partly empty
+// last wave would leave SMs idle for a whole split's time.
 SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim, int per_sm) {
     SplitPlan pl;
     const int64_t tiles = std::max<int64_t>(1, (max_keys + tile - 1) / tile);
     int64_t ns = requested;
     if (ns <= 0) {
         const int sms = sm_count();
-        ns = std::max<int64_t>(1, (int64_t)per_sm * (sms > 0 ? sms : 1) / std::max(1, units));
+        const int64_t wave = (int64_t)per_sm * (sms > 0 ? sms : 1);
+        const int64_t n_units = std::max(1, units);
+        ns = std::max<int64_t>(1, wave / n_units);
         if (batch > 1) {
             const int64_t keys_cap = std::max<int64_t>(tile, kRaggedSplitBytes / (4 * head_dim) / tile * tile);
-            ns = std::max<int64_t>(ns, (max_keys + keys_cap - 1) / keys_cap);
+            const int64_t ns_cap = (max_keys + keys_cap - 1) / keys_cap;
+            if (ns_cap > ns) {
+                const int64_t waves = (n_units * ns_cap + wave - 1) / wave;
+                ns = std::max(ns_cap, waves * wave / n_units);
+            }
         }
     }
     ns = std::min<int64_t>(ns, tiles);
