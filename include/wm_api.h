@@ -315,8 +315,14 @@ wm_status wm_draft_step(const wm_ring *ring, const wm_mem *mem, const void *k_ne
 
 /*
  * Number of key splits an attention call will use, for a cache holding up to
- * max_keys positions per sequence (draft: sink + window).  Depends on the
- * current device's SM count.  Returns 0 on invalid arguments.
+ * max_keys positions per sequence (draft: sink + window).  n_split > 0 is
+ * taken as given (at most one split per key tile).  n_split = 0 plans one
+ * wave of the kernel's resident CTAs over the batch x n_kv_heads (sequence,
+ * KV head) pairs.  With batch > 1 (lengths may differ, only their maximum is
+ * known here) splits are also capped at about 8 MB of K+V each, and a cap
+ * that needs more than one wave is rounded up to fill its last one.  Depends
+ * on the current device's SM count and the kernels' measured residency.
+ * Returns 0 on invalid arguments.
  */
 int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads,
                        int32_t n_q, int32_t head_dim, int64_t max_keys, int32_t n_split);

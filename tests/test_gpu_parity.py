@@ -280,3 +280,18 @@ def test_lse_merge_kernel_matches_oracle():
     out, lse = wm.lse_merge(o, ls)
     ref, ref_lse = oracle.lse_merge(o.double().cpu().numpy(), ls.double().cpu().numpy())
     assert_close("lse_merge", out, lse, ref, ref_lse)
+
+
+def test_split_plan_fills_waves():
+    """Default plans: one wave of resident CTAs for a single sequence; for a
+    batch, the per-split K+V cap rounded up to fill its last wave."""
+    gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # hybrid verify: 2 KV heads, 32 rows at head_dim 256 (one CTA per SM), 1M keys
+    assert wm.plan_splits(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, 0) == sms // 2
+    # two 1M sequences x 8 KV heads, 40 rows at head_dim 128 (one CTA per SM):
+    # the 8 MB cap asks for ceil(1M / 16384) = 64 splits, 1024 CTAs; the count
+    # is raised to the most splits that still fit in ceil(1024 / sms) waves
+    ns = wm.plan_splits(wm.WM_OP_VERIFY, 2, 8, 64, 5, 128, 1 << 20, 0)
+    units, waves = 16, -(-16 * 64 // sms)
+    assert ns >= 64 and units * ns <= waves * sms < units * (ns + 1)
