@@ -295,3 +295,33 @@ def test_split_plan_fills_waves():
     ns = wm.plan_splits(wm.WM_OP_VERIFY, 2, 8, 64, 5, 128, 1 << 20, 0)
     units, waves = 16, -(-16 * 64 // sms)
     assert ns >= 64 and units * ns <= waves * sms < units * (ns + 1)
+
+
+@pytest.mark.parametrize("B,cap,paged", [(3, 20000, False), (16, 6000, True), (17, 3000, False)])
+def test_ragged_batch_split_sizes(B, cap, paged):
+    """Ragged batches with the planned split count: a few long sequences and
+    many short or empty ones, so that most planned splits are empty."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(600 + B)
+    Hkv, G, T, D = 2, 4, 2, 128
+    cpu_gen = torch.Generator().manual_seed(601 + B)
+    lens = torch.randint(0, cap + 1, (B,), generator=cpu_gen).tolist()
+    lens[0], lens[-1] = cap, 1
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev)
+    if paged:
+        page = 64
+        max_pages = (cap + page - 1) // page
+        n_pages = B * max_pages
+        perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(602 + B))
+        block_table = perm.view(B, max_pages).to(torch.int32).to(dev)
+        k = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+        v = rand_bf16((n_pages, Hkv, page, D), gen, dev)
+    else:
+        block_table = None
+        k = rand_bf16((B, Hkv, cap, D), gen, dev)
+        v = rand_bf16((B, Hkv, cap, D), gen, dev)
+    kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), block_table)
+    out, lse = wm.verify_attn(kv, q, D ** -0.5)
+    ref, ref_lse = oracle.verify(oracle_kv(k, v, block_table), q.cpu(), lens, D ** -0.5)
+    assert_close(f"ragged B={B} paged={paged}", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
