@@ -342,6 +342,15 @@ def gpu_arm(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
     clocks = clk.summary()
+    # The same step graph replayed without the flush: the ring stays in L2
+    # from one step to the next (the verify streams its cache evict-first).
+    warm_draft_ms = []
+    if st.ev:
+        for i in range(3 + max(3, args.steps // 2)):
+            st.graph.replay()
+            torch.cuda.synchronize()
+            if i >= 3:
+                warm_draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
     if not st.ev:  # no in-graph events: time the verify alone, same way
         for _ in range(args.steps):
             flush()
@@ -417,6 +426,10 @@ def gpu_arm(args, rank, world, local):
             "draft_kv_bytes_per_step": 2 * B * Hkv * w.slots * D * 2,
             "draft_l2": "L2 flushed before each step; draft steps 2..d re-read the ring (S+W slots) "
                         "mostly from L2, as a decode loop does",
+            "draft_us_per_step_warm_l2": (round(1e3 * sum(warm_draft_ms) / len(warm_draft_ms) / depth, 2)
+                                          if warm_draft_ms else None),
+            "draft_warm_l2": "the same step graph replayed without the flush: the ring stays in L2 from step "
+                             "to step (the verify reads its cache evict-first)",
             "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
             "masw_draft": masw,
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
@@ -619,7 +632,8 @@ def e2e_leg(st: Step, args, world, device) -> dict:
 def oracle_sample(w, depth, inp_host, rows_fraction):
     """One bounded sample of the step on the host: every draft row of the d
     draft steps, and an evenly spaced fraction of the verify rows.  Returns
-    (seconds, scale factor to a whole step, description)."""
+    (seconds spent, seconds per whole step, description, seconds per draft
+    step, seconds per whole verify)."""
     import oracle
 
     B, Hq, T = w.batch, w.n_q_heads, depth + 1
@@ -635,10 +649,11 @@ def oracle_sample(w, depth, inp_host, rows_fraction):
     t1 = time.perf_counter()
     oracle.verify(hist, inp_host["q_verify"], inp_host["lens"], w.scale, rows=rows)
     t_verify = time.perf_counter() - t1
-    per_step = t_draft + t_verify * total_rows / n_rows
+    verify_s = t_verify * total_rows / n_rows
+    per_step = t_draft + verify_s
     desc = (f"all {B * Hq} draft rows x {depth} draft steps + {n_rows}/{total_rows} verify rows "
             f"(scaled x{total_rows / n_rows:.2f}) of {w.name}")
-    return t_draft + t_verify, per_step, desc
+    return t_draft + t_verify, per_step, desc, t_draft / max(1, depth), verify_s
 
 
 def host_inputs(inp):
@@ -650,7 +665,7 @@ def host_inputs(inp):
 def pick_fraction(w, depth, inp_host, budget_s):
     """Verify-row fraction whose oracle time is about ``budget_s`` seconds."""
     probe = 1.0 / (w.batch * (depth + 1) * w.n_q_heads)
-    secs, _, _ = oracle_sample(w, depth, inp_host, probe)
+    secs = oracle_sample(w, depth, inp_host, probe)[0]
     rows_per_s = 1.0 / max(secs, 1e-6)
     frac = min(1.0, budget_s * rows_per_s / (w.batch * (depth + 1) * w.n_q_heads))
     return max(probe, frac)
@@ -663,14 +678,18 @@ def cpu_baseline(st: Step, args, min_seconds: float = 10.0) -> dict:
 
     inp_host = host_inputs(st.inp)
     frac = pick_fraction(st.w, st.d, inp_host, budget_s=min_seconds / 2)
-    total, per_steps, desc = 0.0, [], ""
+    total, per_steps, drafts, verifies, desc = 0.0, [], [], [], ""
     while total < min_seconds:
-        secs, per_step, desc = oracle_sample(st.w, st.d, inp_host, frac)
+        secs, per_step, desc, draft_s, verify_s = oracle_sample(st.w, st.d, inp_host, frac)
         total += secs
         per_steps.append(per_step)
-    return {"value": round(1e6 * sum(per_steps) / len(per_steps), 1), "unit": UNIT,
+        drafts.append(draft_s)
+        verifies.append(verify_s)
+    n = len(per_steps)
+    return {"value": round(1e6 * sum(per_steps) / n, 1), "unit": UNIT,
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{len(per_steps)} x ({desc})", "sample_seconds": round(total, 2)}
+            "sample": f"{n} x ({desc})", "sample_seconds": round(total, 2),
+            "draft_us_per_step": round(1e6 * sum(drafts) / n, 1), "verify_us": round(1e6 * sum(verifies) / n, 1)}
 
 
 def reference_arm(args, rank, world, local):
@@ -694,10 +713,12 @@ def reference_arm(args, rank, world, local):
     frac = pick_fraction(w, depth, inp_host, budget_s=budget)
     for _ in range(args.warmup):
         oracle_sample(w, depth, inp_host, frac)
-    per_steps, secs_total, desc = [], 0.0, ""
+    per_steps, drafts, verifies, secs_total, desc = [], [], [], 0.0, ""
     for _ in range(args.steps):
-        secs, per_step, desc = oracle_sample(w, depth, inp_host, frac)
+        secs, per_step, desc, draft_s, verify_s = oracle_sample(w, depth, inp_host, frac)
         per_steps.append(per_step)
+        drafts.append(draft_s)
+        verifies.append(verify_s)
         secs_total += secs
     us = 1e6 * sum(per_steps) / len(per_steps)
     line = {
@@ -708,7 +729,8 @@ def reference_arm(args, rank, world, local):
         "config": {"workload": w.name, "draft_depth": depth, "verify_positions": depth + 1,
                    "parallelism": "host cores (OpenMP over rows)"},
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "draft_us_per_step": round(1e6 * sum(drafts) / len(drafts), 1),
+                         "verify_us": round(1e6 * sum(verifies) / len(verifies), 1)},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
