@@ -273,6 +273,12 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
             const uint64_t policy = l2_policy_evict_first();
             int issued = 0;
             int32_t last_page = 0;
+            // Paged: the boxes of a split step through its pages in order (a box
+            // never crosses a page), so the page and row of each box advance
+            // without a division per box.  Tile t's boxes serve K_t and V_t.
+            int64_t next_local = 0;                                   // page of the next box, from first_page
+            int next_row = (int)(k_begin - first_page * p.page_size);  // its first row in that page
+            int box_page[2] = {0, 0}, box_row[2] = {0, 0};            // tile t's boxes (TK / box_rows <= 2)
             for (int u = 0; u < 2 * n_tiles; ++u) {
                 const int s = u % C::NSLOT;
                 if (u >= C::NSLOT &&
@@ -286,18 +292,16 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
                 const CUtensorMap *map = (u & 1) ? &tmv : &tmk;
                 const uint32_t dst = sbase + s * C::SLOT_BYTES;
                 const int64_t key0 = k_begin + (int64_t)t * TK;
-                mbar_arrive_expect_tx(bar_full0 + 8 * s, C::SLOT_BYTES);
-                for (int h = 0; h < TK / p.box_rows; ++h) {
-                    const int64_t kh = key0 + (int64_t)h * p.box_rows;
-                    int c_row, c_outer;
-                    if (p.source == KEYS_PAGED) {
-                        if (kh < n_keys) {
-                            const int64_t local = kh / p.page_size - first_page;
+                if (p.source == KEYS_PAGED && (u & 1) == 0) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h * p.box_rows >= TK) break;
+                        if (key0 + (int64_t)h * p.box_rows < n_keys) {
                             int32_t page;
-                            if (local < kTcPageCache) {
-                                page = page_cache[local];
+                            if (next_local < kTcPageCache) {
+                                page = page_cache[next_local];
                             } else {
-                                page = p.block_table[(int64_t)b * p.max_pages + kh / p.page_size];
+                                page = p.block_table[(int64_t)b * p.max_pages + first_page + next_local];
                                 if (page < 0 || page >= p.n_pages) {
                                     tc_report(p.err, WM_DEVERR_BAD_PAGE);
                                     page = 0;
@@ -305,8 +309,24 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
                             }
                             last_page = page;
                         }
-                        c_row = (int)(kh % p.page_size);  // past the end: any valid page, masked later
-                        c_outer = last_page;
+                        box_page[h] = last_page;  // past the end: any valid page, masked later
+                        box_row[h] = next_row;
+                        next_row += p.box_rows;
+                        if (next_row >= p.page_size) {
+                            next_row = 0;
+                            ++next_local;
+                        }
+                    }
+                }
+                mbar_arrive_expect_tx(bar_full0 + 8 * s, C::SLOT_BYTES);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // TK / box_rows boxes: one (128 rows) or two (64)
+                    if (h * p.box_rows >= TK) break;
+                    const int64_t kh = key0 + (int64_t)h * p.box_rows;
+                    int c_row, c_outer;
+                    if (p.source == KEYS_PAGED) {
+                        c_row = box_row[h];
+                        c_outer = box_page[h];
                     } else {
                         c_row = (int)kh;
                         c_outer = b;
