@@ -187,6 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t policy =
                 p.source == KEYS_RING ? l2_policy_evict_normal() : l2_policy_evict_first();
             int issued = 0;
+            // Paged: the tiles of a split step through its pages in order (a tile
+            // never crosses a page), so the page and row advance without a
+            // division, and each tile's block-table entry is loaded one tile ahead.
+            const bool paged = p.source == KEYS_PAGED;
+            int64_t pg = paged ? k_begin / p.page_size : 0;
+            int pg_row = paged ? (int)(k_begin - pg * p.page_size) : 0;
+            int32_t pg_entry = paged ? p.block_table[(int64_t)b * p.max_pages + pg] : 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int s = t % C::STAGES;
                 if (t >= C::STAGES &&
@@ -198,13 +205,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) break;
                 const int64_t key0 = k_begin + (int64_t)t * TK;
                 int c_row, c_outer;
-                if (p.source == KEYS_PAGED) {
-                    int32_t page = p.block_table[(int64_t)b * p.max_pages + key0 / p.page_size];
+                if (paged) {
+                    int32_t page = pg_entry;
+                    c_row = pg_row;
+                    pg_row += TK;
+                    if (pg_row >= p.page_size) {  // the next tile starts the next page
+                        pg_row = 0;
+                        ++pg;
+                        if (t + 1 < n_tiles) pg_entry = p.block_table[(int64_t)b * p.max_pages + pg];
+                    }
                     if (page < 0 || page >= p.n_pages) {
                         report_error(p.err, WM_DEVERR_BAD_PAGE);
                         page = 0;
                     }
-                    c_row = (int)(key0 % p.page_size);
                     c_outer = page;
                 } else {
                     c_row = (int)(key0 >= mem_lo ? key0 - mem_lo : key0);  // a tile is all ring or all memory
