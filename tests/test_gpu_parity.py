@@ -213,11 +213,12 @@ def test_paged_verify_matches_contiguous_oracle():
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("page", [64, 128, 256])
+@pytest.mark.parametrize("page", [64, 128, 192, 256])
 def test_paged_page_sizes_and_short_sequences(D, page):
     """Paged verify over a permuted page pool at several page sizes (128-key
-    boxes when the page holds whole 128-key tiles), with an empty sequence and
-    one shorter than the verify window (its early queries see no key)."""
+    boxes when the page holds whole 128-key tiles; at 192 keys a split may
+    start mid-page), with an empty sequence and one shorter than the verify
+    window (its early queries see no key)."""
     dev = gpu()
     gen = torch.Generator(device=dev).manual_seed(400 + D + page)
     B, Hkv, G, T = 4, 2, 4, 3
@@ -230,15 +231,15 @@ def test_paged_page_sizes_and_short_sequences(D, page):
     v = rand_bf16((n_pages, Hkv, page, D), gen, dev)
     q = rand_bf16((B, T, Hkv * G, D), gen, dev)
     kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), block_table)
-    for ns in (0, 1, 3):
+    ref, ref_lse = oracle.verify(oracle_kv(k, v, block_table), q.cpu(), lens, D ** -0.5)
+    for ns in (0, 1, 3, 5):  # 5: 256-key splits, which start mid-page at 192-key pages
         out, lse = wm.verify_attn(kv, q, D ** -0.5, n_split=ns)
-        ref, ref_lse = oracle.verify(oracle_kv(k, v, block_table), q.cpu(), lens, D ** -0.5)
         assert_close(f"paged D={D} page={page} ns={ns}", out, lse, ref, ref_lse)
     assert wm.get_device_error() == 0
 
 
 @pytest.mark.parametrize("G,T", [(8, 6), (16, 3), (8, 5), (16, 4), (8, 7)])
-@pytest.mark.parametrize("page", [0, 64, 256])
+@pytest.mark.parametrize("page", [0, 64, 192, 256])
 def test_verify_head_dim_256_many_rows(G, T, page):
     """head_dim 256 with 33-64 rows per KV head (the largest tensor-core row
     tiles, where only two K/V staging slots fit): a split of ~10 tiles cycles
@@ -263,7 +264,7 @@ def test_verify_head_dim_256_many_rows(G, T, page):
     kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), block_table)
     hist = oracle_kv(k, v, block_table)
     ref, ref_lse = oracle.verify(hist, q.cpu(), lens, D ** -0.5)
-    for ns in (0, 1, 4):
+    for ns in (0, 1, 4, 12):  # 12: one 128-key tile per split, starting mid-page at 192-key pages
         out, lse = wm.verify_attn(kv, q, D ** -0.5, n_split=ns)
         assert_close(f"verify D=256 G={G} T={T} page={page} ns={ns}", out, lse, ref, ref_lse)
     assert wm.get_device_error() == 0
