@@ -55,22 +55,32 @@ constexpr int kTcPageCache = 256;  // block-table entries of one split kept in s
 // warps would leave too few registers per thread).  More, shorter softmax
 // warps hide the latency of the tensor-memory loads, MUFU and barriers per tile.
 __host__ __device__ constexpr int tc_softmax_warps(int nr) { return nr <= 32 ? 4 * (nr / 8) : 4 * (nr / 16); }
-__host__ __device__ constexpr int tc_threads(int nr) { return (2 + tc_softmax_warps(nr)) * 32; }
+// V tiles in 64-key halves at head_dim 256 with 48 rows (see TcPlan), streamed
+// by one more warp than the other configurations have.
+__host__ __device__ constexpr bool tc_split_v(int d, int nr) { return d == 256 && nr == 48; }
+__host__ __device__ constexpr int tc_threads(int d, int nr) {
+    return (2 + tc_softmax_warps(nr) + (tc_split_v(d, nr) ? 1 : 0)) * 32;
+}
 constexpr float kLazyRescale = 8.f;  // raise the running max only past 2^8
 constexpr float kMaxFloor = -1e30f;  // running-max start, below any finite logit (log2 units)
 
-template <int D, int NR, int NSLOT_, int NPB_>
+// NVS_ > 0: K tiles use the NSLOT_ slots and V tiles are staged separately
+// as 64-key halves in NVS_ half-tile slots; else K and V tiles share the ring.
+template <int D, int NR, int NSLOT_, int NPB_, int NVS_ = 0>
 struct TcLayout {
     static constexpr int TK = kTcKeyTile;
-    static constexpr int NSLOT = NSLOT_, NPB = NPB_;
+    static constexpr int NSLOT = NSLOT_, NPB = NPB_, NVS = NVS_;
     static constexpr int NCH = D / 64;                         // 128-byte column chunks of a row
     static constexpr int NOC = D / 128;                        // O accumulators (M = 128 each)
     static constexpr int REGION = TK * 128;                    // one 64-column chunk of a tile
     static constexpr int SLOT_BYTES = TK * D * 2;              // one K or V tile
+    static constexpr int VREGION = (TK / 2) * 128;             // one 64-column chunk of a V half tile
+    static constexpr int VSLOT_BYTES = (TK / 2) * D * 2;       // one V half tile (64 keys)
+    static constexpr int V_OFF = NSLOT * SLOT_BYTES;
     static constexpr int PT_ROW = NR <= 16 ? 32 : NR <= 32 ? 64 : 128;  // bytes per key row of P^T
     static constexpr int PT_SWIZZLE = NR <= 16 ? 6 : NR <= 32 ? 4 : 2;  // 32B / 64B / 128B swizzle (descriptor code)
     static constexpr int PT_ATOM = PT_ROW * 8;                 // one 8-key swizzle atom
-    static constexpr int Q_OFF = NSLOT * SLOT_BYTES;
+    static constexpr int Q_OFF = V_OFF + NVS * VSLOT_BYTES;
     static constexpr int Q_REGION = NR * 128;
     static constexpr int PT_OFF = Q_OFF + NCH * Q_REGION;      // NPB x (P^T hi, P^T lo)
     static constexpr int PT_BYTES = TK * PT_ROW;
@@ -78,7 +88,7 @@ struct TcLayout {
     static constexpr int FLAG_OFF = RED_OFF + 4 * NR * 4;        // int flags[64]
     static constexpr int BT_OFF = FLAG_OFF + 256;                // int page_cache[kTcPageCache]
     static constexpr int BAR_OFF = BT_OFF + 4 * kTcPageCache;
-    static constexpr int NBAR = 2 * NSLOT + 10;
+    static constexpr int NBAR = 2 * NSLOT + 2 * NVS + 10;
     static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TOTAL = TPTR_OFF + 16 + 1024;
     static constexpr bool FITS = TOTAL <= 227 * 1024;
@@ -90,25 +100,35 @@ struct TcLayout {
 // HBM).  Each takes as many 32 KB slots as let both fit in shared memory.
 __host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 128 && nr == 16; }
 
+// V tiles in 64-key halves at head_dim 256 with 48 rows: the query and P^T
+// buffers leave room for only two 64 KB tile slots, so with a shared ring the
+// next V tile could be requested only after the current P.V completes.  With
+// one K slot and V half slots, a V half waits only for the P.V half that used
+// its slot, and each half is 32 KB of whole key rows.
+
 // Shared-memory plan: the most K/V staging slots (up to 6) that fit with one
 // P^T buffer -- keeping enough HBM requests in flight per SM (well over 100 KB
 // at loaded HBM latency) matters most -- then a second P^T buffer if it fits.
 template <int D, int NR>
 struct TcPlan {
-    static constexpr int NSLOT = tc_two_per_sm(D, NR) ? (2 * TcLayout<D, NR, 3, 1>::TOTAL <= 226 * 1024 ? 3 : 2)
+    static constexpr int NVS = tc_split_v(D, NR) ? 2 : 0;
+    static constexpr int NSLOT = tc_split_v(D, NR) ? 1
+                                 : tc_two_per_sm(D, NR) ? (2 * TcLayout<D, NR, 3, 1>::TOTAL <= 226 * 1024 ? 3 : 2)
                                  : TcLayout<D, NR, 6, 1>::FITS   ? 6
                                  : TcLayout<D, NR, 5, 1>::FITS ? 5
                                  : TcLayout<D, NR, 4, 1>::FITS ? 4
                                  : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
-    static constexpr int NPB = !tc_two_per_sm(D, NR) && TcLayout<D, NR, NSLOT, 2>::FITS ? 2 : 1;
+    static constexpr int NPB = !tc_two_per_sm(D, NR) && TcLayout<D, NR, NSLOT, 2, NVS>::FITS ? 2 : 1;
     static_assert(!tc_two_per_sm(D, NR) || 2 * TcLayout<D, NR, NSLOT, NPB>::TOTAL <= 228 * 1024,
                   "two CTAs per SM must fit in shared memory");
 };
 
 template <int D, int NR>
 struct TcCfg {
-    using L = TcLayout<D, NR, TcPlan<D, NR>::NSLOT, TcPlan<D, NR>::NPB>;
-    static constexpr int NSLOT = L::NSLOT, NPB = L::NPB;
+    using L = TcLayout<D, NR, TcPlan<D, NR>::NSLOT, TcPlan<D, NR>::NPB, TcPlan<D, NR>::NVS>;
+    static constexpr int NSLOT = L::NSLOT, NPB = L::NPB, NVS = L::NVS;
+    static constexpr bool SV = NVS > 0;                        // V staged in half tiles
+    static constexpr int V_OFF = L::V_OFF, VREGION = L::VREGION, VSLOT_BYTES = L::VSLOT_BYTES;
     static constexpr int TK = L::TK, NCH = L::NCH, NOC = L::NOC, REGION = L::REGION;
     static constexpr int SLOT_BYTES = L::SLOT_BYTES;
     static constexpr int PT_ROW = L::PT_ROW, PT_SWIZZLE = L::PT_SWIZZLE, PT_ATOM = L::PT_ATOM;
@@ -117,7 +137,7 @@ struct TcCfg {
     static constexpr int FLAG_OFF = L::FLAG_OFF, BAR_OFF = L::BAR_OFF, TPTR_OFF = L::TPTR_OFF, TOTAL = L::TOTAL;
     static constexpr int BT_OFF = L::BT_OFF;
     static constexpr int NSW = tc_softmax_warps(NR);            // softmax warps
-    static constexpr int THREADS = tc_threads(NR);
+    static constexpr int THREADS = tc_threads(D, NR);
     static constexpr int HR = NR / (NSW / 4);                  // rows per softmax warp
     static constexpr int S_COL = 0;                            // 2 x NR
     static constexpr int O_COL = 2 * NR;                       // NOC x NR
@@ -127,6 +147,7 @@ struct TcCfg {
     static_assert(NR % 16 == 0 && NR >= 16 && NR <= 64, "rows per KV head");
     static_assert(Q_OFF % 1024 == 0 && PT_OFF % 1024 == 0 && PT_BYTES % 1024 == 0, "1024-byte regions");
     static_assert(L::FITS, "shared memory budget");
+    static_assert(!SV || (NVS >= 2 && NSLOT >= 1 && D == 256), "half-tile V staging");
 };
 
 __device__ __forceinline__ void tc_report(int32_t *err, int32_t code) {
@@ -145,7 +166,7 @@ __device__ __forceinline__ bool in_smem(uint32_t lo, uint32_t len, uint32_t base
 }
 
 template <int D, int NR>
-__global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
+__global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const AttnParams p) {
     using C = TcCfg<D, NR>;
@@ -166,7 +187,9 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
     const uint32_t bars = sbase + C::BAR_OFF;
     const uint32_t bar_full0 = bars;                          // [NSLOT]
     const uint32_t bar_empty0 = bars + 8 * C::NSLOT;          // [NSLOT]
-    const uint32_t bar_sfull = bars + 16 * C::NSLOT;          // [2]
+    const uint32_t bar_vfull0 = bars + 16 * C::NSLOT;         // [NVS] (V half tiles)
+    const uint32_t bar_vempty0 = bar_vfull0 + 8 * C::NVS;     // [NVS]
+    const uint32_t bar_sfull = bars + 16 * C::NSLOT + 16 * C::NVS;  // [2]
     const uint32_t bar_sfree = bar_sfull + 16;                // [2]
     const uint32_t bar_pfull = bar_sfree + 16;                // [2]
     const uint32_t bar_odone = bar_pfull + 16;                // [2]
@@ -227,6 +250,10 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
             mbar_init(bar_full0 + 8 * s, 1);
             mbar_init(bar_empty0 + 8 * s, 1);
         }
+        for (int s = 0; s < C::NVS; ++s) {
+            mbar_init(bar_vfull0 + 8 * s, 1);
+            mbar_init(bar_vempty0 + 8 * s, 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull + 8 * i, 1);
             mbar_init(bar_sfree + 8 * i, NSW);
@@ -247,15 +274,16 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tptr;
 
-    if (warp == 0) {
+    if (warp == 0 || (C::SV && warp == 2 + NSW)) {
         // ======================================================== TMA producer
+        // (half-tile V: warp 0 streams K, the last warp V)
         // Paged caches: the whole warp first copies this split's block-table
         // entries into shared memory, so that the lane issuing the copies never
         // waits on a global load per box (entries past the cache are read from
         // global memory as they are needed).
         int32_t *page_cache = reinterpret_cast<int32_t *>(gb + C::BT_OFF);
         const int64_t first_page = p.source == KEYS_PAGED ? k_begin / p.page_size : 0;
-        if (p.source == KEYS_PAGED) {
+        if (warp == 0 && p.source == KEYS_PAGED) {
             const int64_t n_pages_split = (k_end - 1) / p.page_size - first_page + 1;
             for (int i = lane; i < kTcPageCache && i < n_pages_split; i += 32) {
                 int32_t page = p.block_table[(int64_t)b * p.max_pages + first_page + i];
@@ -267,7 +295,93 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
             }
             __syncwarp();
         }
-        if (lane == 0 && n_tiles > 0) {
+        if (C::SV) {  // the V warp reads the block-table cache that warp 0 fills
+            if (warp == 0)
+                named_bar_arrive(2, 64);
+            else
+                named_bar_sync(2, 64);
+        }
+        if (C::SV && lane == 0 && n_tiles > 0) {
+            // Warp 0 streams the K tiles into the tile slots, the V warp the V
+            // tiles as 64-key halves into the half-tile slots, each on its own
+            // barriers, so that neither waits for the other's slots.  Paged
+            // boxes step through the pages as below.
+            const bool is_v = warp != 0;
+            const CUtensorMap *map = is_v ? &tmv : &tmk;
+            prefetch_tensormap(map);
+            const uint64_t policy = l2_policy_evict_first();
+            const int nslot = is_v ? C::NVS : C::NSLOT;
+            const int n_units = is_v ? 2 * n_tiles : n_tiles;
+            const int unit_keys = is_v ? TK / 2 : TK;
+            const int box = is_v ? TK / 2 : p.box_rows;
+            const uint32_t full0 = is_v ? bar_vfull0 : bar_full0;
+            const uint32_t empty0 = is_v ? bar_vempty0 : bar_empty0;
+            const uint32_t slot_bytes = is_v ? C::VSLOT_BYTES : C::SLOT_BYTES;
+            const uint32_t region = is_v ? C::VREGION : C::REGION;
+            const uint32_t area0 = sbase + (is_v ? C::V_OFF : 0);
+            const uint32_t area1 = area0 + nslot * slot_bytes;
+            int issued = 0;
+            int32_t last_page = 0;
+            int64_t next_local = 0;
+            int next_row = (int)(k_begin - first_page * p.page_size);
+            for (int u = 0; u < n_units; ++u) {
+                const int s = u % nslot;
+                if (u >= nslot && !mbar_wait_bounded(empty0 + 8 * s, ((u / nslot) & 1) ^ 1, kWaitLimit)) {
+                    tc_report(p.err, WM_DEVERR_TIMEOUT);
+                    flags[0] = 1;
+                    break;
+                }
+                if (flags[0]) break;
+                const uint32_t dst = area0 + s * slot_bytes;
+                const int64_t key0 = k_begin + (int64_t)u * unit_keys;
+                mbar_arrive_expect_tx(full0 + 8 * s, slot_bytes);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h * box >= unit_keys) break;
+                    const int64_t kh = key0 + (int64_t)h * box;
+                    int c_row, c_outer;
+                    if (p.source == KEYS_PAGED) {
+                        if (kh < n_keys) {
+                            int32_t page;
+                            if (next_local < kTcPageCache) {
+                                page = page_cache[next_local];
+                            } else {
+                                page = p.block_table[(int64_t)b * p.max_pages + first_page + next_local];
+                                if (page < 0 || page >= p.n_pages) {
+                                    tc_report(p.err, WM_DEVERR_BAD_PAGE);
+                                    page = 0;
+                                }
+                            }
+                            last_page = page;
+                        }
+                        c_row = next_row;  // past the end: any valid page, masked later
+                        c_outer = last_page;
+                        next_row += box;
+                        if (next_row >= p.page_size) {
+                            next_row = 0;
+                            ++next_local;
+                        }
+                    } else {
+                        c_row = (int)kh;
+                        c_outer = b;
+                    }
+                    if (!in_smem(dst + (C::NCH - 1) * region + h * box * 128, box * 128, area0, area1) ||
+                        c_row < 0 || c_outer < 0) {
+                        tc_report(p.err, WM_DEVERR_INTERNAL);
+                        flags[0] = 1;
+                        break;
+                    }
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d(dst + c * region + h * box * 128, map, full0 + 8 * s, c * 64, c_row, kvh,
+                                    c_outer, policy);
+                }
+                issued = u + 1;
+            }
+            // Never leave the CTA with bulk copies still landing in its shared memory.
+            for (int u = max(0, issued - nslot); u < issued; ++u)
+                mbar_wait_bounded(full0 + 8 * (u % nslot), (u / nslot) & 1, kWaitLimit);
+        } else if (!C::SV && lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
             const uint64_t policy = l2_policy_evict_first();
@@ -359,18 +473,22 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
             // oldest tile whose P is written -- so that neither waits on the
             // other's inputs.
             int ts = 0, tp = 0;
+            int th = 0;  // half-tile V: the half of tile tp whose P.V is next
             uint32_t idle = 0;
             while (ok && tp < n_tiles) {
                 if (flags[0]) break;
                 bool did = false;
                 if (ts < n_tiles) {
-                    const int uk = 2 * ts, sk = uk % C::NSLOT;
+                    // the K unit of tile ts: 2 ts in the shared ring, or ts in the K ring
+                    const int uk = C::SV ? ts : 2 * ts, sk = uk % C::NSLOT;
                     // A parity test cannot tell "this fill landed" from "the fill
                     // before it has not landed yet" (the parities match), so only
                     // test once the slot's previous unit is known to have landed:
                     // its consumer (S for a K unit, P.V for a V unit) was issued.
+                    // (A K ring holds K units only, consumed in order: always so.)
                     const int prev = uk - C::NSLOT;
-                    const bool prev_in = prev < 0 || ((prev & 1) ? (prev >> 1) < tp : (prev >> 1) < ts);
+                    const bool prev_in =
+                        C::SV || prev < 0 || ((prev & 1) ? (prev >> 1) < tp : (prev >> 1) < ts);
                     if (prev_in && mbar_test(bar_full0 + 8 * sk, (uk / C::NSLOT) & 1) &&
                         (ts < 2 || mbar_test(bar_sfree + 8 * (ts & 1), ((ts - 2) >> 1) & 1))) {
                         tc::fence_after_sync();
@@ -398,7 +516,50 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
                         did = true;
                     }
                 }
-                if (tp < ts) {
+                if (C::SV && tp < ts) {
+                    // P.V of one 64-key V half: the half's slot held an earlier
+                    // half, whose P.V was issued before (halves go in order)
+                    const int uv = 2 * tp + th, sv = uv % C::NVS;
+                    if (mbar_test(bar_pfull + 8 * (tp & 1), (tp >> 1) & 1) &&
+                        mbar_test(bar_vfull0 + 8 * sv, (uv / C::NVS) & 1)) {
+                        tc::fence_after_sync();
+                        const uint32_t a_v = sbase + C::V_OFF + sv * C::VSLOT_BYTES;
+                        const uint32_t pt = sPT + (tp % NPB) * 2 * C::PT_BYTES;
+                        if (!in_smem(a_v, C::VSLOT_BYTES, sbase + C::V_OFF, sbase + C::V_OFF + C::NVS * C::VSLOT_BYTES) ||
+                            !in_smem(pt, 2 * C::PT_BYTES, sPT, sPT + 2 * NPB * C::PT_BYTES)) {
+                            tc_report(p.err, WM_DEVERR_INTERNAL);
+                            ok = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int k4 = 0; k4 < TK / 32; ++k4) {  // 16-key steps within the half
+                            const int kk = th * (TK / 32) + k4;
+                            const uint32_t first = (tp == 0 && kk == 0) ? 0u : 1u;
+                            const uint32_t koff = kk * 2 * C::PT_ATOM;
+                            const uint64_t b_hi =
+                                tc::smem_desc(pt + koff, C::PT_BYTES, C::PT_ATOM, C::PT_SWIZZLE);
+                            const uint64_t b_lo =
+                                tc::smem_desc(pt + C::PT_BYTES + koff, C::PT_BYTES, C::PT_ATOM, C::PT_SWIZZLE);
+#pragma unroll
+                            for (int m = 0; m < C::NOC; ++m) {
+                                const uint64_t a = tc::smem_desc(a_v + 2 * m * C::VREGION + k4 * 2048, C::VREGION,
+                                                                 1024, tc::SWIZZLE_128B);
+                                const uint32_t d_o = tmem + C::O_COL + m * NR;
+                                tc::mma_f16_ss(d_o, a, b_hi, id_pv, first);
+                                tc::mma_f16_ss(d_o, a, b_lo, id_pv, 1u);
+                            }
+                        }
+                        tc::commit(bar_vempty0 + 8 * sv);
+                        if (th == 1) {
+                            tc::commit(bar_odone + 8 * (tp & 1));
+                            ++tp;
+                            th = 0;
+                        } else {
+                            th = 1;
+                        }
+                        did = true;
+                    }
+                } else if (tp < ts) {
                     const int uv = 2 * tp + 1, sv = uv % C::NSLOT;
                     const int prev = uv - C::NSLOT;  // see the K test above
                     const bool prev_in = prev < 0 || ((prev & 1) ? (prev >> 1) < tp : (prev >> 1) < ts);
@@ -647,16 +808,22 @@ __global__ void __launch_bounds__(tc_threads(NR), tc_two_per_sm(D, NR) ? 2 : 1)
                 // The slot's previous unit is older than tile t-1's V, so once
                 // P_{t-1}.V_{t-1} is complete that unit has landed too and the
                 // parity wait below cannot mistake it for this tile's V.
-                const int uv = 2 * t + 1, sv = uv % C::NSLOT;
+                // (with half-tile V: the half holding key kt, whose slot's previous
+                // half belongs to tile t-1 or earlier)
+                const int uv = C::SV ? 2 * t + kt / (TK / 2) : 2 * t + 1;
+                const int nsl = C::SV ? C::NVS : C::NSLOT, sv = uv % nsl;
+                const uint32_t vfull = (C::SV ? bar_vfull0 : bar_full0) + 8 * sv;
                 const bool prev_in =
                     t == 0 || mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit);
-                if (prev_in && mbar_wait_bounded(bar_full0 + 8 * sv, (uv / C::NSLOT) & 1, kWaitLimit)) {
-                    const uint32_t vrow = sbase + sv * C::SLOT_BYTES;
+                if (prev_in && mbar_wait_bounded(vfull, (uv / nsl) & 1, kWaitLimit)) {
+                    const uint32_t vrow = C::SV ? sbase + C::V_OFF + sv * C::VSLOT_BYTES : sbase + sv * C::SLOT_BYTES;
+                    const uint32_t region = C::SV ? C::VREGION : C::REGION;
+                    const int krow = C::SV ? kt % (TK / 2) : kt;
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            st_shared_v4(vrow + c * C::REGION + swz128(kt, j), make_uint4(0u, 0u, 0u, 0u));
+                            st_shared_v4(vrow + c * region + swz128(krow, j), make_uint4(0u, 0u, 0u, 0u));
                 } else {
                     tc_report(p.err, WM_DEVERR_TIMEOUT);
                     flags[0] = 1;

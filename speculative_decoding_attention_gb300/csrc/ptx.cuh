@@ -130,6 +130,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int n_threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
 
+// Arrive on named barrier `id` (n_threads in all) without waiting for it.
+__device__ __forceinline__ void named_bar_arrive(int id, int n_threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
+}
+
 // 2^x and log2(x) with the hardware's approximate units (relative error far
 // below bf16 resolution); ex2 of -inf is +0.
 __device__ __forceinline__ float ex2(float x) {
