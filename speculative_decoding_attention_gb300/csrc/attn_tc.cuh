@@ -55,9 +55,9 @@ constexpr int kTcPageCache = 256;  // block-table entries of one split kept in s
 // warps would leave too few registers per thread).  More, shorter softmax
 // warps hide the latency of the tensor-memory loads, MUFU and barriers per tile.
 __host__ __device__ constexpr int tc_softmax_warps(int nr) { return nr <= 32 ? 4 * (nr / 8) : 4 * (nr / 16); }
-// V tiles in 64-key halves at head_dim 256 with 48 rows (see TcPlan), streamed
+// V tiles in 64-key halves at head_dim 256 with 48 or 64 rows (see TcPlan), streamed
 // by one more warp than the other configurations have.
-__host__ __device__ constexpr bool tc_split_v(int d, int nr) { return d == 256 && nr == 48; }
+__host__ __device__ constexpr bool tc_split_v(int d, int nr) { return d == 256 && nr >= 48; }
 __host__ __device__ constexpr int tc_threads(int d, int nr) {
     return (2 + tc_softmax_warps(nr) + (tc_split_v(d, nr) ? 1 : 0)) * 32;
 }
@@ -100,8 +100,8 @@ struct TcLayout {
 // HBM).  Each takes as many 32 KB slots as let both fit in shared memory.
 __host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 128 && nr == 16; }
 
-// V tiles in 64-key halves at head_dim 256 with 48 rows: the query and P^T
-// buffers leave room for only two 64 KB tile slots, so with a shared ring the
+// V tiles in 64-key halves at head_dim 256 with 48 or 64 rows: the query and
+// P^T buffers leave room for only two 64 KB tile slots, so with a shared ring the
 // next V tile could be requested only after the current P.V completes.  With
 // one K slot and V half slots, a V half waits only for the P.V half that used
 // its slot, and each half is 32 KB of whole key rows.

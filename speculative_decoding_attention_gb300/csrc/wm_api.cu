@@ -514,9 +514,9 @@ wm_status wm_verify_attn(const wm_kv *kv, const void *q, int32_t n_q, int32_t n_
     const int64_t outer = paged ? kv->n_pages : kv->batch;
     const int tile = key_tile(WM_OP_VERIFY, kv->head_dim);
     const int box = paged && kv->page_size % tile ? kKeyTile : tile;  // a box never crosses a page
-    // 48 rows at head dim 256: the tensor-core kernel stages V in 64-key halves
+    // 33-64 rows at head dim 256: the tensor-core kernel stages V in 64-key halves
     const int rows = group * n_q;
-    const int vbox = kv->head_dim == 256 && rows > 32 && rows <= 48 ? kKeyTile : box;
+    const int vbox = kv->head_dim == 256 && rows > 32 ? kKeyTile : box;
     const MapEncoder maps = [kv, inner, outer, box, vbox](CUtensorMap (&m)[4]) {
         if (!encode_kv_map(&m[0], kv->k, kv->head_dim, inner, kv->n_kv_heads, outer, box) ||
             !encode_kv_map(&m[1], kv->v, kv->head_dim, inner, kv->n_kv_heads, outer, vbox))
