@@ -19,6 +19,7 @@ on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -124,11 +125,18 @@ def profiled_traffic(workload: str, depth: int, context=None):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms (200 ms if refused).
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The caller keeps the GPU busy with untimed steps while the sampler starts
+    (``load_until_sampled``) and after the timed region, so every sample is
+    taken under the step's load; ``mark`` brackets the timed region so that
+    the summary also counts the samples taken inside it.
+    """
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, device):
         try:
@@ -137,17 +145,21 @@ class ClockSampler:
             self.gpu = str(device.index or 0)
         self.proc = None
         self.path = None
+        self.window = None
+
+    def _start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval_ms)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+        self.interval_ms = self.INTERVAL_MS
+        self._start()
         return self
 
     def __exit__(self, *exc):
@@ -157,6 +169,31 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+
+    def _count(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def load_until_sampled(self, step, n: int, limit_s: float = 3.0):
+        """Run ``step`` (untimed) until ``n`` more samples have been written."""
+        if self.proc is None:
+            return
+        goal = self._count() + n
+        t0 = time.time()
+        while self._count() < goal and time.time() - t0 < limit_s:
+            if self.proc.poll() is not None and self._count() == 0 and self.interval_ms < 200:
+                self.interval_ms = 200  # this nvidia-smi refused the short interval
+                self._start()
+                if self.proc is None:
+                    return
+            step()
+            torch.cuda.synchronize()
+
+    def mark(self, t_begin: float, t_end: float):
+        self.window = (t_begin, t_end)
 
     def summary(self) -> dict:
         rows = []
@@ -179,12 +216,26 @@ class ClockSampler:
             except ValueError:
                 return None
 
+        def stamp(x):
+            try:
+                return datetime.datetime.strptime(x, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
         mx = [num(r[2]) for r in rows if num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i - 5] for r in rows for i in range(5, 9) if r[i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": reasons, "samples": len(rows), "interval_ms": self.interval_ms,
+               "window": "every sample taken while step graphs run (untimed steps before and after "
+                         "the timed region, and the timed steps)"}
+        if self.window:
+            lo, hi = self.window
+            inside = [r for r in rows if (s := stamp(r[0])) is not None and lo <= s <= hi]
+            out["samples_in_timed_region"] = len(inside)
+            out["timed_region_s"] = round(hi - lo, 4)
+        return out
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -326,9 +377,16 @@ def gpu_arm(args, rank, world, local):
     step_ms, draft_ms, verify_ms = [], [], []
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+
+    def untimed_step():
+        flush()
+        st.graph.replay()
+
     with ClockSampler(device) as clk:
+        clk.load_until_sampled(untimed_step, 3)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_begin = time.time()
         for _ in range(args.steps):
             flush()
             e0.record()
@@ -340,7 +398,10 @@ def gpu_arm(args, rank, world, local):
                 draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
                 verify_ms.append(st.ev[1].elapsed_time(st.ev[2]))
         torch.cuda.synchronize()
+        t_end = time.time()
         barrier(world)
+        clk.mark(t_begin, t_end)
+        clk.load_until_sampled(untimed_step, 2)
     clocks = clk.summary()
     # The same step graph replayed without the flush: the ring stays in L2
     # from one step to the next (the verify streams its cache evict-first).
