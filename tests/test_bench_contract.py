@@ -1,0 +1,82 @@
+"""bench.py's host side on the CPU: the reference arm's JSON line and the
+clock-sample summary (no GPU; the GPU arm is exercised by the GPU runs)."""
+import datetime
+import importlib.util
+import json
+import os
+import subprocess
+import sys
+import time
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def load_bench():
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_4k",
+                        "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is False and d["value"] > 0
+    assert d["config"]["workload"] == "tiny_4k"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def write_samples(path, t0, rows):
+    with open(path, "w") as f:
+        for k, (mhz, reasons) in enumerate(rows):
+            ts = datetime.datetime.fromtimestamp(t0 + 0.02 * k).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+            flags = ["Active" if r else "Not Active" for r in reasons]
+            f.write(f"{ts}, {mhz}, 2070, 900.0, 0x0, " + ", ".join(flags) + "\n")
+
+
+def test_clock_summary_counts_samples_in_the_timed_region(tmp_path):
+    bench = load_bench()
+    clk = bench.ClockSampler(torch.device("cpu"))
+    clk.path = str(tmp_path / "clocks.csv")
+    clk.interval_ms = 20
+    t0 = time.time()
+    quiet = (False, False, False, False)
+    write_samples(clk.path, t0, [(2070, quiet)] * 3 + [(2055, quiet)] * 4 + [(2070, quiet)] * 2)
+    clk.mark(t0 + 0.05, t0 + 0.13)  # samples 3..6
+    s = clk.summary()
+    assert s["samples"] == 9 and s["samples_in_timed_region"] == 4
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070 and s["reasons"] == []
+    assert not os.path.exists(clk.path)  # the summary removes its scratch file
+
+
+@pytest.mark.parametrize("which,name", [(0, "hw_slowdown"), (1, "hw_thermal_slowdown"),
+                                        (2, "sw_thermal_slowdown"), (3, "sw_power_cap")])
+def test_clock_summary_names_each_throttle_reason(tmp_path, which, name):
+    bench = load_bench()
+    clk = bench.ClockSampler(torch.device("cpu"))
+    clk.path = str(tmp_path / "clocks.csv")
+    clk.interval_ms = 20
+    flags = tuple(i == which for i in range(4))
+    write_samples(clk.path, time.time(), [(2070, (False,) * 4), (1800, flags)])
+    assert clk.summary()["reasons"] == [name]
+
+
+def test_clock_summary_without_samples(tmp_path):
+    bench = load_bench()
+    clk = bench.ClockSampler(torch.device("cpu"))
+    clk.path = str(tmp_path / "missing.csv")
+    assert clk.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
