@@ -6,8 +6,8 @@
 //
 // One CTA per (row, 32-column block).  Its 128 threads are 8 column threads
 // (one float4 each) x 16 part groups.  Each thread folds its parts (every
-// 16th) in one pass with a running maximum -- the part's lse and o loads do
-// not depend on each other or on earlier parts, so they are all in flight
+// 16th) in batches of 8 with a running maximum -- a batch's lse and o loads
+// do not depend on each other or on earlier parts, so they are all in flight
 // together -- and the 16 group states (max, sum of weights, weighted o) meet
 // in shared memory.
 //
@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kColThreads = 8;     // float4 columns per CTA -> 32 columns
 constexpr int kPartGroups = 16;
+constexpr int kBatch = 8;         // parts per thread whose loads are in flight together
 constexpr int kMergeThreads = kColThreads * kPartGroups;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -53,31 +54,43 @@ __global__ void __launch_bounds__(kMergeThreads)
     const bool in_cols = col < head_dim;
     const float *op = o_parts + r * (int64_t)n_parts * head_dim + (in_cols ? col : 0);
 
-    // this group's parts, in log2 units: m = max lse, z = sum 2^(lse - m), acc = sum 2^(lse - m) o
+    // this group's parts, in log2 units: m = max lse, z = sum 2^(lse - m), acc = sum 2^(lse - m) o.
+    // Parts are folded kBatch at a time: all of a batch's loads are issued
+    // before any is used, so up to kBatch * kPartGroups parts cost one round
+    // trip to L2.
     float m = -CUDART_INF_F, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = pg; s < n_parts; s += kPartGroups) {
-        const float l = __ldg(ls + s) * kLog2e;
-        const float4 v = in_cols ? __ldg(reinterpret_cast<const float4 *>(op + (int64_t)s * head_dim))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (l == -CUDART_INF_F) continue;  // an empty part: its o is not used
-        if (l > m) {
-            const float c = ex2(m - l);  // 0 while m is -inf
-            z = z * c + 1.f;
-            acc.x = acc.x * c + v.x;
-            acc.y = acc.y * c + v.y;
-            acc.z = acc.z * c + v.z;
-            acc.w = acc.w * c + v.w;
-            m = l;
-        } else {
-            const float w = ex2(l - m);
-            z += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+    for (int s0 = pg; s0 < n_parts; s0 += kBatch * kPartGroups) {
+        float l[kBatch];
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int s = s0 + j * kPartGroups;
+            l[j] = s < n_parts ? __ldg(ls + s) * kLog2e : -CUDART_INF_F;
+            v[j] = s < n_parts && in_cols ? __ldg(reinterpret_cast<const float4 *>(op + (int64_t)s * head_dim))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        float mb = m;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, l[j]);
+        if (mb == -CUDART_INF_F) continue;  // no part with a key yet
+        const float c = ex2(m - mb);         // 0 while m is -inf
+        z *= c;
+        acc.x *= c;
+        acc.y *= c;
+        acc.z *= c;
+        acc.w *= c;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (l[j] == -CUDART_INF_F) continue;  // an empty part: its o was never written
+            const float w = ex2(l[j] - mb);
+            z += w;
+            acc.x += w * v[j].x;
+            acc.y += w * v[j].y;
+            acc.z += w * v[j].z;
+            acc.w += w * v[j].w;
+        }
+        m = mb;
     }
     m_s[pg][ct] = m;
     z_s[pg][ct] = z;
