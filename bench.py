@@ -310,14 +310,18 @@ class Step:
             ev[2].record()
         wm.ring_rollback(self.ring, self.base_len)
 
-    def capture(self, fused: bool = True):
-        """Capture one step in a CUDA graph; returns (graph, in-graph events or None)."""
+    def capture(self, fused: bool = True, events: bool = True):
+        """Capture one step in a CUDA graph; returns (graph, in-graph events or None).
+        With ``events`` the graph also records events before the draft chain,
+        between it and the verify, and after the verify."""
         self.run(fused=fused)  # eager once: kernel attributes, descriptors, first-touch
         torch.cuda.synchronize()
-        try:
-            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
-        except TypeError:
-            ev = None
+        ev = None
+        if events:
+            try:
+                ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+            except TypeError:
+                ev = None
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream())
         graph = torch.cuda.CUDAGraph()
@@ -364,7 +368,10 @@ def gpu_arm(args, rank, world, local):
         workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)
 
     st = Step(w, depth, device, context=args.context)
-    st.capture()
+    # The timed graph holds the step's kernels only; a second capture with
+    # events between the draft chain and the verify gives the breakdown.
+    st.capture(events=False)
+    timed_graph = st.graph
     flush = L2Flush(device)
 
     for _ in range(max(3, args.warmup)):
@@ -390,19 +397,26 @@ def gpu_arm(args, rank, world, local):
         for _ in range(args.steps):
             flush()
             e0.record()
-            st.graph.replay()
+            timed_graph.replay()
             e1.record()
             e1.synchronize()
             step_ms.append(e0.elapsed_time(e1))
-            if st.ev:
-                draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
-                verify_ms.append(st.ev[1].elapsed_time(st.ev[2]))
         torch.cuda.synchronize()
         t_end = time.time()
         barrier(world)
         clk.mark(t_begin, t_end)
         clk.load_until_sampled(untimed_step, 2)
     clocks = clk.summary()
+    # Breakdown: the step captured with in-graph events, replayed the same way.
+    st.capture(events=True)
+    if st.ev:
+        for i in range(max(3, args.warmup) + args.steps):
+            flush()
+            st.graph.replay()
+            torch.cuda.synchronize()
+            if i >= max(3, args.warmup):
+                draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
+                verify_ms.append(st.ev[1].elapsed_time(st.ev[2]))
     # The same step graph replayed without the flush: the ring stays in L2
     # from one step to the next (the verify streams its cache evict-first).
     warm_draft_ms = []
@@ -474,7 +488,7 @@ def gpu_arm(args, rank, world, local):
             "l2": "flushed between timed steps (write of a 2x L2 buffer, then a read of another 2x L2 buffer so "
                   "the flush's dirty lines are written back before the step); each step also reads the full "
                   "KV cache (> L2)",
-            "execution": "one CUDA graph per step", "parallelism": f"replicas x{world}",
+            "execution": "one CUDA graph per step (kernels only; the draft / verify breakdown in detail comes from a second capture with events between them)", "parallelism": f"replicas x{world}",
         },
         "detail": {
             "step_us_median": round(1e3 * sorted(step_ms)[len(step_ms) // 2], 2),
