@@ -247,7 +247,7 @@ wm_status wm_lse_merge(const float *o_parts, const float *lse_parts, int32_t n_p
 /*
  * Draft attention for callers that cannot allocate device memory.
  *
- * The paper has no counterpart: this is a deployment convenience.  Some
+ * Windowed-MTP describes no such call: this is a deployment convenience.  Some
  * callers have no way to obtain the workspace that wm_draft_attn needs --
  * runtimes that reserve all device memory at start-up and refuse any later
  * allocation, plugins hosted by a framework that owns the GPU allocator and
