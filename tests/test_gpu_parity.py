@@ -119,6 +119,38 @@ def test_draft_ring_wraps(D, S, W):
             assert_close(f"draft D={D} S={S} W={W} p={p}", out, lse, ref, ref_lse)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("S,W,n_split", [(4, 1020, 1), (4, 1021, 1), (16, 1500, 1), (16, 2100, 2), (0, 3000, 3)])
+def test_draft_long_splits(D, S, W, n_split):
+    """Splits around and above 1024 ring keys, where a CTA stops staging the
+    split's tags with Q and reads them from global memory a tile ahead; plain
+    and fused-step, with the window part-filled and wrapped."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(250 + D + S + W + n_split)
+    B, Hkv, G = 2, 2, 4
+    n_pos = 2 * (S + W) + 5
+    hk = rand_bf16((B, Hkv, n_pos, D), gen, dev)
+    hv = rand_bf16((B, Hkv, n_pos, D), gen, dev)
+    hist = oracle_kv(hk, hv)
+    scale = 1 / math.sqrt(D)
+    for start in (S + W // 2, n_pos - 3):  # ring part-filled; ring wrapped
+        ring = wm.Ring.create(B, Hkv, D, S, W, dev)
+        wm.ring_fill(ring, wm.KVCache(hk, hv, torch.full((B,), start, dtype=torch.int64, device=dev)))
+        ws = wm.step_workspace(ring, Hkv * G, n_split)
+        for j in range(2):
+            p = start + j
+            q = rand_bf16((B, Hkv * G, D), gen, dev)
+            if j == 0:
+                wm.ring_append(ring, hk[:, :, p].contiguous(), hv[:, :, p].contiguous())
+                out, lse = wm.draft_attn(ring, q, scale, n_split=n_split)
+            else:
+                out, lse = wm.draft_step(ring, hk[:, :, p].contiguous(), hv[:, :, p].contiguous(), q, scale, ws,
+                                         n_split=n_split)
+            ref, ref_lse = oracle.draft(hist, q.cpu(), [p] * B, S, W, scale)
+            assert_close(f"draft D={D} S={S} W={W} ns={n_split} p={p}", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
 def test_draft_with_window_covering_everything_equals_verify():
     """S + W >= p + 1: windowed draft equals full causal attention (single query)."""
     dev = gpu()
