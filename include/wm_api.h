@@ -40,7 +40,9 @@
  *   - head_dim must be 64, 128 or 256; n_q_heads a multiple of n_kv_heads;
  *     G * (query positions) at most 64 rows per KV head; batch * n_kv_heads
  *     at most 65535 for the attention calls and wm_ring_fill, batch at most
- *     65535 for wm_ring_rollback (WM_ERR_UNSUPPORTED otherwise).
+ *     65535 for wm_ring_rollback; a wm_kv holds at most INT32_MAX positions
+ *     per sequence (n_cap, or max_pages * page_size) and at most INT32_MAX
+ *     pages (WM_ERR_UNSUPPORTED otherwise).
  */
 #ifndef WM_API_H
 #define WM_API_H

@@ -206,6 +206,8 @@ wm_status kv_check(const wm_kv *kv, bool need_tile_pages) {
             return WM_ERR_INVALID_ARG;
         if (need_tile_pages && kv->page_size % kKeyTile) return WM_ERR_UNSUPPORTED;  // whole 64-key boxes
         if (kv->n_pages > INT32_MAX) return WM_ERR_UNSUPPORTED;
+        // split lengths are 32-bit: a sequence holds at most INT32_MAX positions
+        if ((int64_t)kv->max_pages * kv->page_size > INT32_MAX) return WM_ERR_UNSUPPORTED;
     } else if (kv->n_cap <= 0 || kv->n_cap > INT32_MAX) {
         return kv->n_cap <= 0 ? WM_ERR_INVALID_ARG : WM_ERR_UNSUPPORTED;
     }

@@ -102,6 +102,9 @@ def test_bad_draft_heads(lib):
     (dict(n_cap=0), 2, 8, wm.WM_ERR_INVALID_ARG),
     (dict(block_table=5 << 20, page_size=16, max_pages=4, n_pages=8), 2, 8, wm.WM_ERR_UNSUPPORTED),
     (dict(block_table=5 << 20, page_size=64, max_pages=0, n_pages=8), 2, 8, wm.WM_ERR_INVALID_ARG),
+    (dict(block_table=5 << 20, page_size=1 << 16, max_pages=1 << 15, n_pages=8), 2, 8,
+     wm.WM_ERR_UNSUPPORTED),                                                  # 2^31 positions per sequence
+    (dict(n_cap=1 << 31), 2, 8, wm.WM_ERR_UNSUPPORTED),
 ])
 def test_bad_verify_shapes(lib, over, n_q, hq, status):
     s = _kv(**over)
