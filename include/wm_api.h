@@ -148,6 +148,8 @@ typedef struct wm_kv {
  * writes k_new[b], v_new[b] into slot(p), sets pos_tag[b][slot(p)] = p and
  * n_seen[b] = p + 1.
  *   k_new, v_new  [batch][n_kv_heads][head_dim] bf16.
+ * Tags are int32, so p must lie in [0, INT32_MAX): any other n_seen[b]
+ * records WM_DEVERR_BAD_LENGTH and appends nothing for b.
  */
 wm_status wm_ring_append(const wm_ring *ring, const void *k_new, const void *v_new, void *stream);
 
@@ -301,9 +303,9 @@ wm_status wm_draft_attn_static(const wm_ring *ring, const void *q, int32_t n_q_h
  *                 partials always pass through the merge, which commits
  *                 n_seen -- 256-byte aligned; no initial contents needed.
  * out, lse and the ring are bit-identical to wm_ring_append followed by
- * wm_draft_attn (wm_draft_attn_mem) with the same n_split.  A negative
- * n_seen[b] records WM_DEVERR_BAD_LENGTH, appends nothing for b and gives its
- * rows out = 0, lse = -inf.
+ * wm_draft_attn (wm_draft_attn_mem) with the same n_split.  An n_seen[b]
+ * outside [0, INT32_MAX) (tags are int32) records WM_DEVERR_BAD_LENGTH,
+ * appends nothing for b and gives its rows out = 0, lse = -inf.
  */
 wm_status wm_draft_step(const wm_ring *ring, const wm_mem *mem, const void *k_new, const void *v_new,
                         const void *q, int32_t n_q_heads, float scale, int32_t n_split, void *out,

@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int64_t new_slot = -1;  // STEP: ring slot receiving position qpos0
     if (p.source == KEYS_RING) {
-        if (seen < 0) {
+        if (seen < 0 || (STEP && seen >= INT32_MAX)) {  // STEP: p must fit an int32 tag
             if (threadIdx.x == 0) report_error(p.err, WM_DEVERR_BAD_LENGTH);
             seen = STEP ? -1 : 0;  // STEP: nothing is appended, every key is masked
         }

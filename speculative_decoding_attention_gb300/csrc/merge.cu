@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (commit_n_seen && blockIdx.y == 0 && tid == 0 && r % rows_per_seq == 0) {
         const int64_t b = r / rows_per_seq;
         const int64_t seen = commit_n_seen[b];
-        if (seen >= 0) commit_n_seen[b] = seen + 1;  // a negative count was reported, nothing appended
+        // a count the attention kernel reported (negative, or past an int32 tag) appended nothing
+        if (seen >= 0 && seen < INT32_MAX) commit_n_seen[b] = seen + 1;
     }
     const float *ls = lse_parts + r * n_parts;
     const int ct = tid % kColThreads, pg = tid / kColThreads;

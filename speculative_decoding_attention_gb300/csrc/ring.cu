@@ -41,7 +41,7 @@ __global__ void ring_append_kernel(uint4 *rk, uint4 *rv, int32_t *tag, int64_t *
     const int b = blockIdx.x;
     const int n_slots = sink + window;
     const int64_t p = n_seen[b];
-    if (p < 0) {
+    if (p < 0 || p >= INT32_MAX) {  // tags are int32: the last position a ring can hold is INT32_MAX - 1
         if (threadIdx.x == 0) report(err, WM_DEVERR_BAD_LENGTH);
         return;
     }

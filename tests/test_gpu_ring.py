@@ -165,3 +165,25 @@ def test_bad_length_sets_device_error():
     q = torch.zeros((1, 1, 1, 64), dtype=torch.bfloat16, device=dev)
     wm.verify_attn(wm.KVCache(k, k, torch.tensor([129], device=dev)), q, 1.0)
     assert wm.get_device_error() == 1
+
+
+@pytest.mark.parametrize("bad", [-1, 2 ** 31 - 1, 2 ** 33])
+def test_append_past_int32_tags_is_refused(bad):
+    """Tags are int32: an append at a position that does not fit one (or at a
+    negative one) is recorded and leaves that sequence's ring untouched."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(31)
+    B, Hkv, D, S, W = 2, 2, 64, 4, 16
+    ring = wm.Ring.create(B, Hkv, D, S, W, dev)
+    hk = rand_bf16((B, Hkv, 40, D), gen, dev)
+    wm.ring_fill(ring, wm.KVCache(hk, hk, torch.tensor([30, 30], device=dev)))
+    before = (ring.k.clone(), ring.v.clone(), ring.pos_tag.clone())
+    ring.n_seen[1] = bad
+    kn, vn = rand_bf16((B, Hkv, D), gen, dev), rand_bf16((B, Hkv, D), gen, dev)
+    wm.ring_append(ring, kn, vn)
+    assert wm.get_device_error() == 1  # WM_DEVERR_BAD_LENGTH
+    assert ring.n_seen.tolist() == [31, bad]
+    for new, old in zip((ring.k, ring.v, ring.pos_tag), before):
+        assert torch.equal(new[1], old[1])
+    s = slot_rule(30, S, W)
+    assert int(ring.pos_tag[0, s]) == 30 and torch.equal(ring.k[0, :, s], kn[0])

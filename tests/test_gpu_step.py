@@ -150,18 +150,20 @@ def test_step_graph_replays_advance_the_ring():
     assert wm.get_device_error() == 0
 
 
-def test_step_negative_n_seen_is_reported_and_skipped():
-    """A negative n_seen is bad device data: recorded, nothing appended for that
-    sequence, its rows 0 / -inf; the other sequence steps normally."""
+@pytest.mark.parametrize("bad", [-5, 2 ** 31 - 1, 2 ** 40])
+def test_step_bad_n_seen_is_reported_and_skipped(bad):
+    """An n_seen that is negative or does not fit an int32 tag is bad device
+    data: recorded, nothing appended for that sequence, its rows 0 / -inf; the
+    other sequence steps normally."""
     B, Hkv, G, D, S, W, lens = 2, 2, 4, 128, 4, 256, [1000, 1000]
     dev, hk, hv, ring, qs = setup(B, Hkv, G, D, S, W, lens, 1, seed=9)
-    ring.n_seen[1] = -5
+    ring.n_seen[1] = bad
     tags_before = ring.pos_tag.clone()
     ws = wm.step_workspace(ring, Hkv * G)
     out, lse = wm.draft_step(ring, gather_pos(hk, lens, 0), gather_pos(hv, lens, 0), qs[0], 1.0 / D ** 0.5, ws)
     torch.cuda.synchronize()
     assert wm.get_device_error() == 1  # WM_DEVERR_BAD_LENGTH
-    assert ring.n_seen.tolist() == [1001, -5]
+    assert ring.n_seen.tolist() == [1001, bad]
     assert torch.equal(ring.pos_tag[1], tags_before[1])
     assert bool((out[1] == 0).all()) and bool(torch.isneginf(lse[1]).all())
     ref, ref_lse = oracle.draft(oracle_kv(hk, hv), qs[0].cpu(), [1000, 1000], S, W, 1.0 / D ** 0.5)
