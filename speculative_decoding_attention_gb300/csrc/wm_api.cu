@@ -60,10 +60,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Encoded tensor maps of recent calls.  A map is a pure function of the
+// base address and the view's shape (it owns nothing), so a decode loop that
+// calls with the same buffers every step reuses the encoding.
+struct MapCacheEntry {
+    bool used = false;
+    const void *base = nullptr;
+    int head_dim = 0, heads = 0, box_rows = 0;
+    int64_t inner = 0, outer = 0;
+    CUtensorMap map;
+};
+constexpr int kMapCacheSize = 64;
+
 // A 4-d view [outer][heads][inner][D] of bf16 rows, read in boxes of
 // 64 columns x box_rows rows with the 128-byte swizzle.
 bool encode_kv_map(CUtensorMap *map, const void *base, int head_dim, int64_t inner, int heads, int64_t outer,
                    int box_rows) {
+    static MapCacheEntry cache[kMapCacheSize];
+    static std::mutex mu;
+    uint64_t h = reinterpret_cast<uintptr_t>(base) >> 4;
+    for (const uint64_t x : {(uint64_t)head_dim, (uint64_t)inner, (uint64_t)heads, (uint64_t)outer,
+                             (uint64_t)box_rows})
+        h = (h ^ x) * 0x100000001b3ull;
+    MapCacheEntry &slot = cache[(h ^ (h >> 29)) % kMapCacheSize];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (slot.used && slot.base == base && slot.head_dim == head_dim && slot.inner == inner &&
+            slot.heads == heads && slot.outer == outer && slot.box_rows == box_rows) {
+            *map = slot.map;
+            return true;
+        }
+    }
     auto encode = tensor_map_encoder();
     if (!encode) return false;
     const cuuint64_t row = (cuuint64_t)head_dim * 2;
@@ -74,7 +101,17 @@ bool encode_kv_map(CUtensorMap *map, const void *base, int head_dim, int64_t inn
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
                               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    slot.used = true;
+    slot.base = base;
+    slot.head_dim = head_dim;
+    slot.inner = inner;
+    slot.heads = heads;
+    slot.outer = outer;
+    slot.box_rows = box_rows;
+    slot.map = *map;
+    return true;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -105,8 +105,15 @@ def _check(status: int, what: str) -> None:
         raise WmError(status, what)
 
 
+# The current stream's handle without building a Stream object (a third of a
+# short call's host time otherwise); the public query where it is missing.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int | None:
     if stream is None:
+        if _raw_current_stream is not None:
+            return _raw_current_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 

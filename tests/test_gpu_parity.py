@@ -358,3 +358,27 @@ def test_ragged_batch_split_sizes(B, cap, paged):
     ref, ref_lse = oracle.verify(oracle_kv(k, v, block_table), q.cpu(), lens, D ** -0.5)
     assert_close(f"ragged B={B} paged={paged}", out, lse, ref, ref_lse)
     assert wm.get_device_error() == 0
+
+
+def test_reused_buffers_and_shapes():
+    """Calls that reuse an address with another shape, or a shape at another
+    address, each get their own tensor map: every result matches the oracle."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(777)
+    D, Hkv, G, T = 128, 2, 4, 3
+    store = rand_bf16((2 * Hkv * 1024 * D,), gen, dev)
+    vstore = rand_bf16((2 * Hkv * 1024 * D,), gen, dev)
+    other_k = rand_bf16((1, Hkv, 1024, D), gen, dev)
+    other_v = rand_bf16((1, Hkv, 1024, D), gen, dev)
+    cases = [  # (k, v, lens): the same storage as [2, Hkv, 1024, D] and as [1, Hkv, 2048, D]
+        (store.view(2, Hkv, 1024, D), vstore.view(2, Hkv, 1024, D), [1000, 700]),
+        (store.view(1, Hkv, 2048, D), vstore.view(1, Hkv, 2048, D), [1900]),
+        (other_k, other_v, [1024]),
+        (store.view(2, Hkv, 1024, D), vstore.view(2, Hkv, 1024, D), [1000, 700]),
+    ]
+    for i, (k, v, lens) in enumerate(cases):
+        q = rand_bf16((len(lens), T, Hkv * G, D), gen, dev)
+        out, lse = wm.verify_attn(wm.KVCache(k, v, torch.tensor(lens, device=dev)), q, D ** -0.5)
+        ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), lens, D ** -0.5)
+        assert_close(f"case {i}", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
