@@ -19,7 +19,10 @@
  *     lse and split partials are fp32; positions/lengths int64; tags and page
  *     indices int32.  Every tensor is dense row-major in the documented shape.
  *   - Ownership: every pointer is caller-owned DEVICE memory unless stated;
- *     the library allocates nothing and keeps no per-call state.
+ *     the library allocates no device memory.  Its only state across calls
+ *     is host-side: the TMA descriptors of recent calls.  A descriptor depends
+ *     only on an address and a shape and owns nothing, so freeing or reusing
+ *     a buffer needs no notice.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
  *     default stream).  Every call only enqueues work on that stream and
  *     returns without synchronising; positions and lengths are read on the
