@@ -777,6 +777,7 @@ def cpu_baseline(st: Step, args, min_seconds: float = 10.0) -> dict:
     of CPU work have run; reported per whole step."""
     import oracle
 
+    oracle.set_num_threads(len(os.sched_getaffinity(0)))  # every host core this process may use
     inp_host = host_inputs(st.inp)
     frac = pick_fraction(st.w, st.d, inp_host, budget_s=min_seconds / 2)
     total, per_steps, drafts, verifies, desc = 0.0, [], [], [], ""
@@ -803,6 +804,9 @@ def reference_arm(args, rank, world, local):
             barrier(world)
             return
     oracle.build()
+    # The launcher may cap each rank at one OpenMP thread; only this rank
+    # works, so it takes every host core it may run on.
+    oracle.set_num_threads(len(os.sched_getaffinity(0)))
     w = workloads.get(args.workload)
     depth = args.depth if args.depth is not None else (
         workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)

@@ -79,6 +79,8 @@ def _load(plant: int = 0) -> ctypes.CDLL:
         for f in (lib.wmo_verify, lib.wmo_draft, lib.wmo_draft_mem, lib.wmo_attend_subset, lib.wmo_lse_merge):
             f.restype = ctypes.c_int
         lib.wmo_num_threads.restype = ctypes.c_int
+        lib.wmo_set_num_threads.argtypes = [ctypes.c_int]
+        lib.wmo_set_num_threads.restype = None
         _libs[plant] = lib
         return lib
 
@@ -257,3 +259,8 @@ def lse_merge(o_parts, lse_parts):
 def num_threads() -> int:
     """Host threads the oracle's OpenMP loops use."""
     return int(_load().wmo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Host threads for the oracle's OpenMP loops from now on."""
+    _load().wmo_set_num_threads(int(n))

@@ -215,6 +215,16 @@ int wmo_num_threads(void)
 #endif
 }
 
+/* Threads for the OpenMP loops from now on (n > 0; ignored without OpenMP). */
+void wmo_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Verification attention.
  * q: [batch][T][Hq][D] bf16; seq_lens: [batch] (N_b, the verify tokens' own
  * K/V being the last T cache entries).  rows: indices into the flattened
