@@ -241,3 +241,20 @@ def test_library_has_no_torch_dependency(lib):
     # The C ABI is plain pointers and sizes: the shared object links no torch.
     needed = _needed_libraries(wm.library_path())
     assert needed and not any("torch" in n or "c10" in n for n in needed), needed
+
+
+def test_split_calls_without_enough_workspace(lib):
+    """Split draft and verify calls check their workspace on the host: missing,
+    misaligned or short -> WM_ERR_WORKSPACE, nothing launched (no device here)."""
+    P = ctypes.c_void_p
+    q, out = P(1 << 24), P(1 << 25)
+    need_v = wm.workspace_size(wm.WM_OP_VERIFY, 1, 2, 8, 2, 128, 4096, 4)
+    need_d = wm.workspace_size(wm.WM_OP_DRAFT, 1, 2, 8, 1, 128, 260, 4)
+    assert need_v > 0 and need_d > 0
+    s, r = _kv(), _ring()
+    for ws, nbytes in [(None, need_v), (P((1 << 26) + 16), need_v), (P(1 << 26), need_v - 1)]:
+        assert lib.wm_verify_attn(ctypes.byref(s), q, 2, 8, 1.0, 4, out, None, ws, nbytes, None) == \
+            wm.WM_ERR_WORKSPACE
+    for ws, nbytes in [(None, need_d), (P((1 << 26) + 16), need_d), (P(1 << 26), need_d - 1)]:
+        assert lib.wm_draft_attn(ctypes.byref(r), q, 8, 1.0, 4, out, None, ws, nbytes, None) == \
+            wm.WM_ERR_WORKSPACE
