@@ -80,3 +80,36 @@ def test_clock_summary_without_samples(tmp_path):
     clk = bench.ClockSampler(torch.device("cpu"))
     clk.path = str(tmp_path / "missing.csv")
     assert clk.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+
+def test_reference_arm_under_two_ranks():
+    """Under torchrun with two ranks only rank 0 prints (one line), and it runs
+    the oracle on every host core even though the launcher caps OpenMP
+    threads per rank."""
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+                        "--workload", "tiny_4k", "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
+
+
+def test_packed_buffers_are_aligned_views():
+    bench = load_bench()
+    buf, views = bench._packed([("a", (3, 1, 16, 256), torch.bfloat16), ("l", (3, 1, 16), torch.float32),
+                                ("c", (1, 4, 16, 256), torch.bfloat16)], torch.device("cpu"), pinned=False)
+    base = buf.data_ptr()
+    for name, t in views.items():
+        assert t.is_contiguous() and (t.data_ptr() - base) % 256 == 0
+    # the views do not overlap and stay inside the buffer
+    ends = sorted((t.data_ptr() - base, t.data_ptr() - base + t.numel() * t.element_size()) for t in views.values())
+    assert all(a[1] <= b[0] for a, b in zip(ends, ends[1:])) and ends[-1][1] <= buf.numel()
