@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/wm_api.h"
+#include "wm_internal.h"
 
 namespace {
 
@@ -38,7 +39,10 @@ void *static_scratch_ptr() {
 extern "C" wm_status wm_draft_attn_static(const wm_ring *ring, const void *q, int32_t n_q_heads,
                                           float scale, int32_t n_split, void *out, float *lse,
                                           void *stream) {
-    if (!ring || n_q_heads <= 0 || n_split < 0) return WM_ERR_INVALID_ARG;
+    // The same host-side checks as wm_draft_attn, first: a bad argument is
+    // reported as such, never as a scratch-size problem.
+    const int32_t args = wm::draft_args_status(ring, q, n_q_heads, scale, n_split, out, lse);
+    if (args != WM_OK) return static_cast<wm_status>(args);
     const size_t need = wm_workspace_size(WM_OP_DRAFT, ring->batch, ring->n_kv_heads, n_q_heads, 1,
                                           ring->head_dim, (int64_t)ring->sink + ring->window, n_split);
     if (need == (size_t)-1) return WM_ERR_INVALID_ARG;

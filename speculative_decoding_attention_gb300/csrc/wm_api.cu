@@ -478,6 +478,23 @@ static wm_status draft_setup(const wm_ring *ring, const wm_mem *mem, const void 
     return WM_OK;
 }
 
+}  // extern "C"
+
+namespace wm {
+
+int32_t draft_args_status(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
+                          const void *out, const float *lse) {
+    AttnParams p;
+    MapEncoder maps;
+    int64_t keys = 0;
+    return draft_setup(ring, nullptr, q, n_q_heads, scale, n_split, const_cast<void *>(out),
+                       const_cast<float *>(lse), p, maps, keys);
+}
+
+}  // namespace wm
+
+extern "C" {
+
 wm_status wm_draft_attn(const wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
                         void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
     AttnParams p;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+struct wm_ring;  // include/wm_api.h
+
 namespace wm {
 
 // Key source of an attention launch.
@@ -148,5 +150,11 @@ cudaError_t launch_ring_rollback(int32_t *tag, int64_t *n_seen, int batch, int n
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n_parts,
                              int64_t rows, int head_dim, void *out, float *lse_out,
                              int64_t *commit_n_seen, int rows_per_seq, cudaStream_t stream);
+
+// The host-side argument checks of wm_draft_attn alone (ring, query, heads,
+// scale, split count, output alignment): a wm_status code, WM_OK when they pass.
+// Nothing is planned, encoded or launched.
+int32_t draft_args_status(const ::wm_ring *ring, const void *q, int32_t n_q_heads, float scale, int32_t n_split,
+                          const void *out, const float *lse);
 
 }  // namespace wm

@@ -300,14 +300,20 @@ def _workspace(nbytes: int, device, workspace: torch.Tensor | None) -> tuple[int
 _keepalive: list[torch.Tensor] = []
 
 
+def _new_out(shape, dtype, device) -> torch.Tensor:
+    """Output buffer of a call that was given none.  Uninitialised: every
+    element is written by the call."""
+    return torch.empty(tuple(shape), dtype=dtype, device=device)
+
+
 def draft_attn(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 0, out=None, lse=None,
                workspace=None, stream=None):
     """Sink + window draft attention of q [B, Hq, D]; returns (out bf16, lse fp32)."""
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = _new_out(q.shape, torch.bfloat16, q.device)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = _new_out((B, Hq), torch.float32, q.device)
     need = workspace_size(WM_OP_DRAFT, B, ring.n_kv_heads, Hq, 1, D, ring.sink + ring.window, n_split)
     ws, ws_bytes = _workspace(need, q.device, workspace)
     r = ring.c()
@@ -340,9 +346,9 @@ def draft_step(ring: Ring, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Te
     when ``mem`` is given: the query then also attends to the memory slots)."""
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = _new_out(q.shape, torch.bfloat16, q.device)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = _new_out((B, Hq), torch.float32, q.device)
     r = ring.c()
     m = mem.c() if mem is not None else None
     _check(load().wm_draft_step(ctypes.byref(r), ctypes.byref(m) if m is not None else None,
@@ -361,9 +367,9 @@ def draft_attn_mem(ring: Ring, mem: Mem, q: torch.Tensor, scale: float, n_split:
     0..mem.count[b]-1 (memory-augmented draft); returns (out bf16, lse fp32)."""
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = _new_out(q.shape, torch.bfloat16, q.device)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = _new_out((B, Hq), torch.float32, q.device)
     need = workspace_size(WM_OP_DRAFT_MEM, B, ring.n_kv_heads, Hq, 1, D, mem_keys(ring, mem), n_split)
     ws, ws_bytes = _workspace(need, q.device, workspace)
     r, m = ring.c(), mem.c()
@@ -397,9 +403,9 @@ def draft_attn_static(ring: Ring, q: torch.Tensor, scale: float, n_split: int = 
     overlap on the GPU share that array and race; keep them on one stream."""
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = _new_out(q.shape, torch.bfloat16, q.device)
     if lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = _new_out((B, Hq), torch.float32, q.device)
     r = ring.c()
     _check(load().wm_draft_attn_static(ctypes.byref(r), _dev(q, torch.bfloat16, "q"), Hq, float(scale),
                                        n_split, _dev(out, torch.bfloat16, "out"),
@@ -413,9 +419,9 @@ def verify_attn(kv: KVCache, q: torch.Tensor, scale: float, n_split: int = 0, ou
     """Full-context causal attention of q [B, T, Hq, D]; returns (out bf16, lse fp32)."""
     B, T, Hq, D = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = _new_out(q.shape, torch.bfloat16, q.device)
     if lse is None:
-        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+        lse = _new_out((B, T, Hq), torch.float32, q.device)
     need = workspace_size(WM_OP_VERIFY, B, kv.n_kv_heads, Hq, T, D, kv.capacity, n_split)
     ws, ws_bytes = _workspace(need, q.device, workspace)
     s = kv.c()
@@ -429,9 +435,9 @@ def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out=None, lse=None
     """Merge partials o_parts [rows, n_parts, D] fp32 with lse_parts [rows, n_parts]."""
     rows, n_parts, D = o_parts.shape
     if out is None:
-        out = torch.empty((rows, D), dtype=torch.bfloat16, device=o_parts.device)
+        out = _new_out((rows, D), torch.bfloat16, o_parts.device)
     if lse is None:
-        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+        lse = _new_out((rows,), torch.float32, o_parts.device)
     _check(load().wm_lse_merge(_dev(o_parts, torch.float32, "o_parts"), _dev(lse_parts, torch.float32,
                                                                              "lse_parts"),
                                n_parts, rows, D, _dev(out, torch.bfloat16, "out"),

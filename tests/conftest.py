@@ -3,7 +3,8 @@ import sys
 
 import pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(ROOT)
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -24,4 +25,21 @@ def _clear_device_error(request):
 
             wm_build.build()
             wm.get_device_error()
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _nan_filled_outputs(request, monkeypatch):
+    """In GPU tests, every output buffer the binding allocates starts as NaN,
+    so that an output row a kernel leaves unwritten fails the parity check
+    instead of passing on whatever the allocator returned."""
+    if request.node.get_closest_marker("gpu") is not None:
+        import torch
+
+        from speculative_decoding_attention_gb300 import wm
+
+        def nan_out(shape, dtype, device):
+            return torch.full(tuple(shape), float("nan"), dtype=dtype, device=device)
+
+        monkeypatch.setattr(wm, "_new_out", nan_out)
     yield

@@ -258,3 +258,23 @@ def test_split_calls_without_enough_workspace(lib):
     for ws, nbytes in [(None, need_d), (P((1 << 26) + 16), need_d), (P(1 << 26), need_d - 1)]:
         assert lib.wm_draft_attn(ctypes.byref(r), q, 8, 1.0, 4, out, None, ws, nbytes, None) == \
             wm.WM_ERR_WORKSPACE
+
+
+def test_static_scratch_draft_reports_bad_arguments_first(lib):
+    """wm_draft_attn_static runs wm_draft_attn's host checks before it looks
+    at its scratch size: a bad argument is WM_ERR_INVALID_ARG from both, even
+    when the plan would also not fit the scratch array."""
+    P = ctypes.c_void_p
+    big = _ring(batch=64, n_kv_heads=8, window=8192, sink=16)  # a plan far beyond the scratch array
+    cases = [
+        (big, 8 * 8 + 3, 1.0, P(16), P(16)),          # query heads not a multiple of the KV heads
+        (big, 64, float("nan"), P(16), P(16)),         # non-finite scale
+        (big, 64, 1.0, P(17), P(16)),                  # misaligned q
+        (big, 64, 1.0, P(16), P(18)),                  # misaligned out
+        (_ring(batch=64, n_kv_heads=8, window=0), 64, 1.0, P(16), P(16)),  # empty window
+        (_ring(batch=64, n_kv_heads=8, head_dim=96), 64, 1.0, P(16), P(16)),
+    ]
+    for r, hq, scale, q, out in cases:
+        a = lib.wm_draft_attn(ctypes.byref(r), q, hq, scale, 0, out, None, None, 0, None)
+        s = lib.wm_draft_attn_static(ctypes.byref(r), q, hq, scale, 0, out, None, None)
+        assert a == wm.WM_ERR_INVALID_ARG and s == wm.WM_ERR_INVALID_ARG, (hq, scale, a, s)

@@ -149,8 +149,8 @@ def test_fused_step_with_memory_in_a_graph():
     kn = torch.stack([hk[b, :, n] for b, n in enumerate(lens)]).contiguous()
     vn = torch.stack([hv[b, :, n] for b, n in enumerate(lens)]).contiguous()
     q = rand_bf16((B, Hkv * G, D), gen, dev)
-    out = torch.empty_like(q)
-    lse = torch.empty((B, Hkv * G), dtype=torch.float32, device=dev)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hkv * G), float("nan"), dtype=torch.float32, device=dev)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -168,6 +168,8 @@ def test_fused_step_with_memory_in_a_graph():
         kn.copy_(torch.stack([hk[b, :, n + j] for b, n in enumerate(lens)]))
         vn.copy_(torch.stack([hv[b, :, n + j] for b, n in enumerate(lens)]))
         q.copy_(rand_bf16((B, Hkv * G, D), gen, dev))
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
         g.replay()
         torch.cuda.synchronize()
         ref, ref_lse = oracle.draft_mem(hist, mhist, [2 + j], q.cpu(), [lens[0] + j], S, W, D ** -0.5)

@@ -124,8 +124,8 @@ def test_step_graph_replays_advance_the_ring():
     scale = D ** -0.5
     ws = wm.step_workspace(ring, Hkv * G)
     kn, vn, q = gather_pos(hk, lens, 0), gather_pos(hv, lens, 0), qs[0].clone()
-    out = torch.empty_like(q)
-    lse = torch.empty((B, Hkv * G), dtype=torch.float32, device=dev)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hkv * G), float("nan"), dtype=torch.float32, device=dev)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):  # warm-up outside the graph: plans and attributes are cached
@@ -142,6 +142,8 @@ def test_step_graph_replays_advance_the_ring():
         kn.copy_(gather_pos(hk, lens, j))
         vn.copy_(gather_pos(hv, lens, j))
         q.copy_(qs[j])
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
         g.replay()
         torch.cuda.synchronize()
         ref, ref_lse = oracle.draft(hist, q.cpu(), [lens[0] + j], S, W, scale)
