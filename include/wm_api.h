@@ -359,6 +359,25 @@ const char *wm_status_string(wm_status status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t wm_version(void);
 
+/*
+ * Test support for the pipeline-wait timeout path (no counterpart on the
+ * pages).  Every wait inside the attention kernels is bounded: after a limit
+ * of polls the kernel records WM_DEVERR_TIMEOUT in the device error word,
+ * stops its remaining work, waits (again bounded) for its own copies in
+ * flight and returns, so a lost arrival can never hang the GPU.  This call
+ * makes that path reachable on purpose: after it, the attention launches made
+ * by the calling host thread through the mma.sync kernels (every draft call;
+ * verification at head_dim 64) have their producer stop issuing copies at key
+ * tile `stall_tile` of each split (a tile that then never arrives) and give up
+ * a wait after `wait_polls` polls (about 0.1 us each, or more: a poll may
+ * suspend the thread briefly).  stall_tile = -1 restores the defaults
+ * (no stall, the production limit of 2^22 polls).  Outputs of a stalled call
+ * are undefined; the context stays usable and the next call is normal.
+ * Returns WM_ERR_INVALID_ARG for stall_tile < -1 or wait_polls = 0 with a stall.
+ * Not for production use.
+ */
+wm_status wm_set_test_stall(int32_t stall_tile, uint32_t wait_polls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -195,9 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pg_row = paged ? (int)(k_begin - pg * p.page_size) : 0;
             int32_t pg_entry = paged ? p.block_table[(int64_t)b * p.max_pages + pg] : 0;
             for (int t = 0; t < n_tiles; ++t) {
+                if (t == p.stall_tile) break;  // tests of the timeout path only
                 const int s = t % C::STAGES;
                 if (t >= C::STAGES &&
-                    !mbar_wait_bounded(bar_empty + 8 * s, ((t / C::STAGES) & 1) ^ 1, kWaitLimit)) {
+                    !mbar_wait_bounded(bar_empty + 8 * s, ((t / C::STAGES) & 1) ^ 1, p.wait_limit)) {
                     report_error(p.err, WM_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Never leave the CTA with bulk copies still landing in its shared memory.
             for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-                mbar_wait_bounded(bar_full + 8 * (t % C::STAGES), (t / C::STAGES) & 1, kWaitLimit);
+                mbar_wait_bounded(bar_full + 8 * (t % C::STAGES), (t / C::STAGES) & 1, p.wait_limit);
         }
         return;
     }
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tags_global && t + 1 < n_tiles) fetch_tags(k_begin + (int64_t)(t + 1) * TK, tg_nxt, tg1_nxt);
         const int s = t % C::STAGES;
         const int buf = t & 1;
-        if (!*abort_flag && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, kWaitLimit)) {
+        if (!*abort_flag && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
             report_error(p.err, WM_DEVERR_TIMEOUT);
             *abort_flag = 1;
         }

@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             int next_row = (int)(k_begin - first_page * p.page_size);
             for (int u = 0; u < n_units; ++u) {
                 const int s = u % nslot;
-                if (u >= nslot && !mbar_wait_bounded(empty0 + 8 * s, ((u / nslot) & 1) ^ 1, kWaitLimit)) {
+                if (u >= nslot && !mbar_wait_bounded(empty0 + 8 * s, ((u / nslot) & 1) ^ 1, p.wait_limit)) {
                     tc_report(p.err, WM_DEVERR_TIMEOUT);
                     flags[0] = 1;
                     break;
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             }
             // Never leave the CTA with bulk copies still landing in its shared memory.
             for (int u = max(0, issued - nslot); u < issued; ++u)
-                mbar_wait_bounded(full0 + 8 * (u % nslot), (u / nslot) & 1, kWaitLimit);
+                mbar_wait_bounded(full0 + 8 * (u % nslot), (u / nslot) & 1, p.wait_limit);
         } else if (!C::SV && lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             for (int u = 0; u < 2 * n_tiles; ++u) {
                 const int s = u % C::NSLOT;
                 if (u >= C::NSLOT &&
-                    !mbar_wait_bounded(bar_empty0 + 8 * s, ((u / C::NSLOT) & 1) ^ 1, kWaitLimit)) {
+                    !mbar_wait_bounded(bar_empty0 + 8 * s, ((u / C::NSLOT) & 1) ^ 1, p.wait_limit)) {
                     tc_report(p.err, WM_DEVERR_TIMEOUT);
                     flags[0] = 1;
                     break;
@@ -460,14 +460,14 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
                 issued = u + 1;
             }
             for (int u = max(0, issued - C::NSLOT); u < issued; ++u)
-                mbar_wait_bounded(bar_full0 + 8 * (u % C::NSLOT), (u / C::NSLOT) & 1, kWaitLimit);
+                mbar_wait_bounded(bar_full0 + 8 * (u % C::NSLOT), (u / C::NSLOT) & 1, p.wait_limit);
         }
     } else if (warp == 1) {
         // ======================================================== MMA issuer
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t id_s = tc::idesc_bf16(128, NR, 0, 0);
             constexpr uint32_t id_pv = tc::idesc_bf16(128, NR, 1, 1);
-            bool ok = mbar_wait_bounded(bar_qfull, 0, kWaitLimit);
+            bool ok = mbar_wait_bounded(bar_qfull, 0, p.wait_limit);
             // Issue whichever product is ready -- S for the next tile (its K
             // landed and its tensor-memory buffer is free) or P.V for the
             // oldest tile whose P is written -- so that neither waits on the
@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
                 }
                 if (did) {
                     idle = 0;
-                } else if (++idle > kWaitLimit) {
+                } else if (++idle > p.wait_limit) {
                     ok = false;
                 } else if (idle > 64) {
                     __nanosleep(32);
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
                 flags[0] = 1;
             }
             tc::commit(bar_final);  // every MMA issued above has completed once this fires
-            mbar_wait_bounded(bar_final, 0, kWaitLimit);
+            mbar_wait_bounded(bar_final, 0, p.wait_limit);
         }
     } else {
         // ======================================================== softmax warps
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             }
             float s[HR];
             bool live = !warp_aborted(flags);
-            if (live && !mbar_wait_bounded(bar_sfull + 8 * (t & 1), (t >> 1) & 1, kWaitLimit)) {
+            if (live && !mbar_wait_bounded(bar_sfull + 8 * (t & 1), (t >> 1) & 1, p.wait_limit)) {
                 tc_report(p.err, WM_DEVERR_TIMEOUT);
                 flags[0] = 1;
             }
@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
                 }
                 if (t > 0) {
                     // O holds tiles 0..t-1 at the old maximum: wait for P_{t-1}.V_{t-1}, then rescale
-                    if (!flags[0] && !mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit)) {
+                    if (!flags[0] && !mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, p.wait_limit)) {
                         tc_report(p.err, WM_DEVERR_TIMEOUT);
                         flags[0] = 1;
                     }
@@ -784,7 +784,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             }
             // the P^T buffer of this tile was last read by P_{t-NPB}.V_{t-NPB}
             if (t >= NPB && !(NPB == 1 && o_stable) && !flags[0] &&
-                !mbar_wait_bounded(bar_odone + 8 * ((t - NPB) & 1), ((t - NPB) >> 1) & 1, kWaitLimit)) {
+                !mbar_wait_bounded(bar_odone + 8 * ((t - NPB) & 1), ((t - NPB) >> 1) & 1, p.wait_limit)) {
                 tc_report(p.err, WM_DEVERR_TIMEOUT);
                 flags[0] = 1;
             }
@@ -814,8 +814,8 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
                 const int nsl = C::SV ? C::NVS : C::NSLOT, sv = uv % nsl;
                 const uint32_t vfull = (C::SV ? bar_vfull0 : bar_full0) + 8 * sv;
                 const bool prev_in =
-                    t == 0 || mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, kWaitLimit);
-                if (prev_in && mbar_wait_bounded(vfull, (uv / nsl) & 1, kWaitLimit)) {
+                    t == 0 || mbar_wait_bounded(bar_odone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, p.wait_limit);
+                if (prev_in && mbar_wait_bounded(vfull, (uv / nsl) & 1, p.wait_limit)) {
                     const uint32_t vrow = C::SV ? sbase + C::V_OFF + sv * C::VSLOT_BYTES : sbase + sv * C::SLOT_BYTES;
                     const uint32_t region = C::SV ? C::VREGION : C::REGION;
                     const int krow = C::SV ? kt % (TK / 2) : kt;
@@ -837,7 +837,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
 
         // ---- epilogue: this thread owns tensor-memory lane d = 32*q4 + lane of every O block
         if (n_tiles > 0 && !flags[0] &&
-            !mbar_wait_bounded(bar_odone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, kWaitLimit)) {
+            !mbar_wait_bounded(bar_odone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, p.wait_limit)) {
             tc_report(p.err, WM_DEVERR_TIMEOUT);
             flags[0] = 1;
         }

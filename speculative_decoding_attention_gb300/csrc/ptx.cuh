@@ -125,9 +125,33 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one bf16x2 pair per
+// thread in the mma fragment layout (thread 4g + t holds row g, columns 2t
+// and 2t + 1): afterwards the thread holds the same positions of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ void named_bar_sync(int id, int n_threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over its n_threads participants:
+// every participant gets the same answer.
+__device__ __forceinline__ bool named_bar_sync_or(int id, int n_threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n_threads)
+        : "memory");
+    return r != 0;
 }
 
 // Arrive on named barrier `id` (n_threads in all) without waiting for it.

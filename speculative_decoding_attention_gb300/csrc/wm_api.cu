@@ -16,6 +16,12 @@ namespace {
 
 __device__ int32_t g_device_error;  // first device-side data error (WM_DEVERR_*)
 
+// Pipeline-wait settings of the attention launches made by this host thread
+// (wm_set_test_stall): the default poll limit and no stall, except in tests of
+// the timeout path.
+thread_local uint32_t t_wait_limit = kWaitLimit;
+thread_local int32_t t_stall_tile = -1;
+
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRows = 64;  // query rows per KV head (4 m-tiles of 16)
 constexpr int64_t kMaxUnits = 65535;  // (sequence, KV head) pairs: the launch grid's y extent
@@ -129,6 +135,10 @@ struct SplitPlan {
 // few megabytes once per step; it is latency-bound, and the mma.sync kernel's
 // 64-key tiles give twice as many CTAs with a shorter fixed cost per CTA.
 bool use_tc_kernel(int op, int head_dim) { return op == WM_OP_VERIFY && head_dim != 64; }
+// The draft with at most 8 query rows per KV head (every GQA group up to 8)
+// runs on the keys-as-M kernel: the rows are the MMA's N, so no padding rows,
+// and each compute warp owns its keys of a tile end to end.
+bool use_draft_kernel(int op, int rows) { return op == WM_OP_DRAFT && rows <= kDraftRowsMax; }
 int key_tile(int op, int head_dim) { return use_tc_kernel(op, head_dim) ? kTcTile : kKeyTile; }
 
 // K+V bytes per split when a batch may be ragged (see plan_splits).
@@ -140,12 +150,24 @@ constexpr int64_t kRaggedSplitBytes = 8ll << 20;
 int ctas_per_sm(int op, int head_dim, int rows) {
     static std::mutex mu;
     static int cache[kMaxDevices][3][4][2] = {};
+    static int draft_cache[kMaxDevices][3] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
     const int mt = std::min(4, std::max(1, (rows + 15) / 16));
     const int oi = op == WM_OP_VERIFY ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
+    if (use_draft_kernel(op, rows)) {
+        int &nd = draft_cache[dev][di];
+        if (!nd) {
+            auto query = [&](bool step) {
+                return di == 0 ? draft_blocks_per_sm_d64(step)
+                     : di == 1 ? draft_blocks_per_sm_d128(step) : draft_blocks_per_sm_d256(step);
+            };
+            nd = std::max(1, std::min(query(false), query(true)));
+        }
+        return nd;
+    }
     int &n = cache[dev][di][mt - 1][oi];
     if (!n && use_tc_kernel(op, head_dim)) {
         n = std::max(1, head_dim == 128 ? attn_tc_blocks_per_sm_d128(16 * mt) : attn_tc_blocks_per_sm_d256(16 * mt));
@@ -206,6 +228,14 @@ size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
 cudaError_t launch_attn_any(int op, const CUtensorMap (&maps)[4], const AttnParams &p, bool step,
                             cudaStream_t st) {
     const int m_tiles = (p.rows + 15) / 16;
+    if (use_draft_kernel(op, p.rows)) {
+        switch (p.head_dim) {
+            case 64: return launch_draft_d64(maps[0], maps[1], maps[2], maps[3], p, step, st);
+            case 128: return launch_draft_d128(maps[0], maps[1], maps[2], maps[3], p, step, st);
+            case 256: return launch_draft_d256(maps[0], maps[1], maps[2], maps[3], p, step, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (!step && use_tc_kernel(op, p.head_dim)) {
         return p.head_dim == 128 ? launch_attn_tc_d128(maps[0], maps[1], p, 16 * m_tiles, st)
                                  : launch_attn_tc_d256(maps[0], maps[1], p, 16 * m_tiles, st);
@@ -285,6 +315,13 @@ const char *wm_status_string(wm_status s) {
 }
 
 int32_t wm_version(void) { return 100; }
+
+wm_status wm_set_test_stall(int32_t stall_tile, uint32_t wait_polls) {
+    if (stall_tile < -1 || (stall_tile >= 0 && wait_polls == 0)) return WM_ERR_INVALID_ARG;
+    t_stall_tile = stall_tile;
+    t_wait_limit = stall_tile < 0 ? kWaitLimit : wait_polls;
+    return WM_OK;
+}
 
 int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
                        int32_t head_dim, int64_t max_keys, int32_t n_split) {
@@ -410,6 +447,8 @@ static wm_status run_attention(int op, AttnParams &p, const MapEncoder &encode_m
     }
     p.err = device_error_ptr();
     if (!p.err) return WM_ERR_CUDA;
+    p.wait_limit = t_wait_limit;
+    p.stall_tile = t_stall_tile;
     CUtensorMap maps[4];
     if (!encode_maps(maps)) return WM_ERR_CUDA;
     cudaError_t e = launch_attn_any(op, maps, p, step, st);

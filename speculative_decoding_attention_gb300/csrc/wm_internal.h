@@ -75,6 +75,11 @@ struct AttnParams {
     const int64_t *mem_count;  // [B]; NULL: no memory slots
     int64_t mem_cap;           // slots the memory store holds per (sequence, KV head)
     int64_t mem_base;          // first key index of the memory region (ring tiles x 64)
+    // pipeline waits: polls before a wait is declared lost, and (tests of the
+    // timeout path only) the key tile at which the producer stops issuing
+    // copies, -1 for none
+    uint32_t wait_limit;
+    int32_t stall_tile;
 };
 
 // Launch the attention kernel for head dim D (defined in attn_d<D>.cu).  mk/mv
@@ -85,6 +90,21 @@ cudaError_t launch_attn_d128(const CUtensorMap &k, const CUtensorMap &v, const C
                              const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
 cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
                              const CUtensorMap &mv, const AttnParams &p, int m_tiles, cudaStream_t stream);
+
+// Keys-as-M draft kernel (draft_d<D>.cu) for up to kDraftRowsMax query rows per
+// KV head: the plain draft attention, or (step) the fused draft step, which
+// always writes split partials.
+constexpr int kDraftRowsMax = 8;
+cudaError_t launch_draft_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                             const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+cudaError_t launch_draft_d128(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                              const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+cudaError_t launch_draft_d256(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
+                              const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+// Resident CTAs per SM of that kernel (0 if unknown).
+int draft_blocks_per_sm_d64(bool step);
+int draft_blocks_per_sm_d128(bool step);
+int draft_blocks_per_sm_d256(bool step);
 
 // Resident CTAs per SM of the mma.sync attention kernel for head dim D with
 // m_tiles row tiles (step: the fused draft-step instance); 0 if unknown.

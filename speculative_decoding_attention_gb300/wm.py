@@ -23,7 +23,7 @@ DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait tim
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
             "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step", "wm_draft_attn_mem",
-            "wm_mem_append", "wm_mem_rollback")
+            "wm_mem_append", "wm_mem_rollback", "wm_set_test_stall")
 STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
 
 _lib = None
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
         lib.wm_status_string.argtypes = [I32]
         lib.wm_status_string.restype = ctypes.c_char_p
         lib.wm_version.restype = I32
+        lib.wm_set_test_stall.argtypes = [I32, ctypes.c_uint32]
+        lib.wm_set_test_stall.restype = I32
         for name in ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_draft_attn_static",
                      "wm_verify_attn", "wm_lse_merge", "wm_get_device_error"):
             getattr(lib, name).restype = I32
@@ -443,6 +445,14 @@ def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out=None, lse=None
                                n_parts, rows, D, _dev(out, torch.bfloat16, "out"),
                                _dev(lse, torch.float32, "lse"), _stream(stream)), "wm_lse_merge")
     return out, lse
+
+
+def set_test_stall(stall_tile: int, wait_polls: int = 0) -> None:
+    """Tests of the timeout path only: make this thread's mma.sync attention
+    launches stop issuing copies at key tile ``stall_tile`` of each split and
+    give up a wait after ``wait_polls`` polls (``stall_tile=-1`` restores the
+    defaults).  See wm_set_test_stall in include/wm_api.h."""
+    _check(load().wm_set_test_stall(int(stall_tile), int(wait_polls)), "wm_set_test_stall")
 
 
 def get_device_error(stream=None) -> int:

@@ -278,3 +278,10 @@ def test_static_scratch_draft_reports_bad_arguments_first(lib):
         a = lib.wm_draft_attn(ctypes.byref(r), q, hq, scale, 0, out, None, None, 0, None)
         s = lib.wm_draft_attn_static(ctypes.byref(r), q, hq, scale, 0, out, None, None)
         assert a == wm.WM_ERR_INVALID_ARG and s == wm.WM_ERR_INVALID_ARG, (hq, scale, a, s)
+
+
+def test_test_stall_hook_rejects_bad_settings(lib):
+    assert lib.wm_set_test_stall(-2, 100) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_set_test_stall(0, 0) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_set_test_stall(3, 100) == wm.WM_OK
+    assert lib.wm_set_test_stall(-1, 0) == wm.WM_OK
