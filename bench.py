@@ -14,7 +14,7 @@ Default workload: 1M-token context, full-attention layer of a hybrid target
 (GQA 8, head_dim 256, S=4, W=4096), draft depth 3.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
-on a bounded sample of the same workload instead.
+on whole steps of the same workload instead.
 """
 from __future__ import annotations
 
@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--depth", type=int, default=None, help="draft depth d (verify T = d + 1)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other 1M-context configurations measured beside the headline")
     ap.add_argument("--context", type=int, default=None,
                     help="shorter context, same recipe (small cases for profiler captures; not a bench line)")
     return ap.parse_args()
@@ -124,19 +126,55 @@ def profiled_traffic(workload: str, depth: int, context=None):
     return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 20 ms (200 ms if refused).
+# NVML clock sampler, run as its own process (no GIL shared with the timing
+# loop): samples the SM clock, its maximum and the clock-event reasons every
+# interval until terminated; one line per sample, CLOCK_MONOTONIC seconds
+# first, so the parent can tell which samples fall inside its timed region.
+_NVML_SAMPLER = r"""
+import ctypes, sys, time
+uuid, interval = sys.argv[1].encode(), float(sys.argv[2])
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(3)
+h = ctypes.c_void_p()
+if nv.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid), ctypes.byref(h)) != 0:
+    sys.exit(4)
+reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+out = sys.stdout
+print("ready", flush=True)
+while True:
+    t = time.monotonic()
+    ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0
+    ok = ok and nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+    ok = ok and reasons(h, ctypes.byref(rs)) == 0
+    if ok:
+        out.write(f"{t:.6f},{sm.value},{mx.value},{rs.value}\n")
+        out.flush()
+    time.sleep(interval)
+"""
 
-    The caller keeps the GPU busy with untimed steps while the sampler starts
-    (``load_until_sampled``) and after the timed region, so every sample is
-    taken under the step's load; ``mark`` brackets the timed region so that
-    the summary also counts the samples taken inside it.
+# clock-event reason bits (NVML) and the names the JSON line uses
+_REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+
+class ClockSampler:
+    """SM clocks and throttle reasons while the step's graphs run.
+
+    Preferred: NVML queried from a separate process every 0.5 ms, so that even
+    a timed region of a few milliseconds holds several samples.  Fallback:
+    ``nvidia-smi -lms 20``.  The caller keeps the GPU busy with untimed steps
+    while the sampler starts (``load_until_sampled``) and after the timed
+    region, so every sample is taken under the step's load; ``mark``
+    brackets the timed region (``time.monotonic()`` seconds) so that the
+    summary also counts the samples taken inside it.
     """
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     INTERVAL_MS = 20
+    NVML_INTERVAL_MS = 0.5
 
     def __init__(self, device):
         try:
@@ -146,8 +184,12 @@ class ClockSampler:
         self.proc = None
         self.path = None
         self.window = None
+        self.source = None
+        self.interval_ms = self.INTERVAL_MS
 
-    def _start(self):
+    def _start_smi(self):
+        self.source = "nvidia-smi"
+        self.interval_ms = self.INTERVAL_MS
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -155,11 +197,36 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
+    def _start_nvml(self) -> bool:
+        if not self.gpu.startswith("GPU-"):
+            return False
+        try:
+            proc = subprocess.Popen([sys.executable, "-c", _NVML_SAMPLER, self.gpu, str(self.NVML_INTERVAL_MS / 1e3)],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return False
+        first = proc.stdout.readline()
+        if first.strip() != "ready":
+            proc.kill()
+            proc.wait()
+            return False
+        self.proc, self.source, self.interval_ms = proc, "nvml", self.NVML_INTERVAL_MS
+        self.rows = []
+        import threading
+
+        def drain():  # the reader thread only appends lines (no GPU work, no timing)
+            for line in proc.stdout:
+                self.rows.append(line)
+
+        self.reader = threading.Thread(target=drain, daemon=True)
+        self.reader.start()
+        return True
+
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        self.interval_ms = self.INTERVAL_MS
-        self._start()
+        if not self._start_nvml():
+            self._start_smi()
         return self
 
     def __exit__(self, *exc):
@@ -169,8 +236,14 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.source == "nvml":
+            self.reader.join(timeout=5)
+            with open(self.path, "w") as f:
+                f.writelines(self.rows)
 
     def _count(self) -> int:
+        if self.source == "nvml":
+            return len(self.rows)
         try:
             with open(self.path) as f:
                 return sum(1 for _ in f)
@@ -184,31 +257,34 @@ class ClockSampler:
         goal = self._count() + n
         t0 = time.time()
         while self._count() < goal and time.time() - t0 < limit_s:
-            if self.proc.poll() is not None and self._count() == 0 and self.interval_ms < 200:
+            if self.source == "nvidia-smi" and self.proc.poll() is not None and self._count() == 0 \
+                    and self.interval_ms < 200:
                 self.interval_ms = 200  # this nvidia-smi refused the short interval
-                self._start()
-                if self.proc is None:
+                self.proc = None
+                try:
+                    self.proc = subprocess.Popen(
+                        ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                         "--format=csv,noheader,nounits", "-lms", "200"], stdout=open(self.path, "w"),
+                        stderr=subprocess.DEVNULL)
+                except OSError:
                     return
             step()
             torch.cuda.synchronize()
 
     def mark(self, t_begin: float, t_end: float):
+        """The timed region, in time.monotonic() seconds."""
         self.window = (t_begin, t_end)
 
-    def summary(self) -> dict:
-        rows = []
+    def _parse(self):
+        """(monotonic time or None, sm MHz, max MHz, set of reason names) per sample."""
+        out = []
         try:
-            for line in open(self.path):
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = open(self.path).read().splitlines()
         except OSError:
-            pass
+            return out
         finally:
             if self.path and os.path.exists(self.path):
                 os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
 
         def num(x):
             try:
@@ -216,25 +292,40 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        def stamp(x):
-            try:
-                return datetime.datetime.strptime(x, "%Y/%m/%d %H:%M:%S.%f").timestamp()
-            except ValueError:
-                return None
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 4:  # nvml: t, sm, max, reason bits
+                t, sm, mx, bits = num(parts[0]), num(parts[1]), num(parts[2]), int(num(parts[3]) or 0)
+                out.append((t, sm, mx, {name for bit, name in _REASON_BITS.items() if bits & bit}))
+            elif len(parts) >= 9:  # nvidia-smi csv: wall-clock stamp, mapped onto monotonic time
+                try:
+                    wall = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    t = wall - (time.time() - time.monotonic())
+                except ValueError:
+                    t = None
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+                out.append((t, num(parts[1]), num(parts[2]),
+                            {names[i - 5] for i in range(5, 9) if parts[i].lower() == "active"}))
+        return out
 
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i - 5] for r in rows for i in range(5, 9) if r[i].lower() == "active"})
+    def summary(self) -> dict:
+        rows = self._parse()
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [r[1] for r in rows if r[1] is not None]
+        mx = [r[2] for r in rows if r[2] is not None]
+        reasons = sorted(set().union(*(r[3] for r in rows)))
         out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-               "reasons": reasons, "samples": len(rows), "interval_ms": self.interval_ms,
+               "reasons": reasons, "samples": len(rows), "interval_ms": self.interval_ms, "source": self.source,
                "window": "every sample taken while step graphs run (untimed steps before and after "
                          "the timed region, and the timed steps)"}
         if self.window:
             lo, hi = self.window
-            inside = [r for r in rows if (s := stamp(r[0])) is not None and lo <= s <= hi]
+            inside = [r for r in rows if r[0] is not None and lo <= r[0] <= hi]
             out["samples_in_timed_region"] = len(inside)
             out["timed_region_s"] = round(hi - lo, 4)
+            if inside:
+                out["sm_mhz_timed_region"] = statistics.median(r[1] for r in inside if r[1] is not None)
         return out
 
 
@@ -331,6 +422,14 @@ class Step:
         self.graph, self.ev = graph, ev
         return graph, ev
 
+    def release(self):
+        """Drop the graphs and device buffers of this workload."""
+        self.graph = self.ev = None
+        for name in ("inp", "kv", "ring", "base_len", "d_out", "d_lse", "v_out", "v_lse", "d_ws", "s_ws", "v_ws"):
+            setattr(self, name, None)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
 
 class L2Flush:
     """Flush the L2 between timed steps: write a buffer of twice the L2, then
@@ -351,6 +450,130 @@ class L2Flush:
 
         self.wbuf.zero_()
         torch.sum(self.rbuf, dim=0, out=self.sink)
+
+
+def workload_config(w, depth: int, context, world: int) -> dict:
+    """The workload a line reports on: the same keys in the GPU arm and the
+    reference arm (how the GPU arm runs it goes under ``detail``)."""
+    return {
+        "workload": w.name, "batch": w.batch,
+        "context": (context if context else w.context) if not w.ragged else f"U[{w.ragged[0]}, {w.ragged[1]}] seeded",
+        "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "sink": w.sink,
+        "window": w.window, "draft_depth": depth, "verify_positions": depth + 1,
+        "kv_layout": f"paged ({w.page_size}-token pages)" if w.page_size else "contiguous",
+        "l2": "flushed between timed steps (write of a 2x L2 buffer, then a read of another 2x L2 buffer so the "
+              "flush's dirty lines are written back before the step); each step also reads the full KV cache (> L2)",
+        "parallelism": f"replicas x{world}",
+    }
+
+
+def step_bytes(st: "Step") -> tuple[int, int]:
+    """Algorithmic HBM bytes of one verify launch and of one draft step."""
+    w = st.w
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    sum_n = sum(st.inp.seq_lens_host)
+    verify_bytes = 2 * Hkv * D * 2 * sum_n + 2 * (B * st.T * Hq * D * 2) + B * st.T * Hq * 4
+    draft_bytes = 2 * B * Hkv * w.slots * D * 2 + 2 * (B * Hq * D * 2) + B * Hq * 4
+    return verify_bytes, draft_bytes
+
+
+def time_graph(graph, flush, n_warm: int, n: int, ev=None):
+    """Replay ``graph`` n_warm + n times with the L2 flushed before each replay;
+    mean milliseconds of the last n replays, timed by CUDA events around the
+    replay, or (``ev``) by the graph's own in-graph events (list of intervals)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ms = []
+    for i in range(n_warm + n):
+        flush()
+        if ev is None:
+            e0.record()
+        graph.replay()
+        if ev is None:
+            e1.record()
+            e1.synchronize()
+        else:
+            torch.cuda.synchronize()
+        if i >= n_warm:
+            ms.append(e0.elapsed_time(e1) if ev is None else [ev[k].elapsed_time(ev[k + 1]) for k in range(len(ev) - 1)])
+    return ms
+
+
+def breakdown(st: "Step", flush, args) -> tuple[float, float]:
+    """Mean draft-chain and verify milliseconds from a capture of the step with
+    events between them (the events cost time themselves, so this graph is never
+    the one the step time comes from)."""
+    st.capture(events=True)
+    if not st.ev:
+        return None, None
+    ms = time_graph(st.graph, flush, max(3, args.warmup), args.steps, ev=st.ev)
+    return sum(m[0] for m in ms) / len(ms), sum(m[1] for m in ms) / len(ms)
+
+
+def extra_1m_line(name: str, depth: int, device, flush, args, peak: float) -> dict:
+    """Step, verify and draft of another 1M-context configuration, measured like
+    the headline (graph of the step's kernels; L2 flushed between steps)."""
+    w = workloads.get(name)
+    st = Step(w, depth, device)
+    st.capture(events=False)
+    step_ms = time_graph(st.graph, flush, max(3, args.warmup), args.steps)
+    draft_ms, verify_ms = breakdown(st, flush, args)
+    vb, db = step_bytes(st)
+    out = {"step_us": round(1e3 * sum(step_ms) / len(step_ms), 2)}
+    if verify_ms:
+        vg = vb / (verify_ms * 1e-3) / 1e9
+        dg = db * depth / (draft_ms * 1e-3) / 1e9
+        out.update({"verify_us": round(1e3 * verify_ms, 2), "verify_gbs": round(vg, 1),
+                    "verify_frac_of_hbm": round(vg / peak, 4),
+                    "draft_us_per_step": round(1e3 * draft_ms / depth, 2), "draft_gbs": round(dg, 1),
+                    "draft_frac_of_hbm": round(dg / peak, 4), "draft_kv_bytes_per_step": db,
+                    "draft_splits": st.d_splits, "verify_splits": st.v_splits})
+    st.release()
+    return out
+
+
+def launch_floors(w, device, flush, args) -> dict:
+    """Measured floors of a dependent chain of draft-step launches, as graphs
+    of d launches with the L2 flushed before each replay (per launch, us):
+    ``empty_kernel``: a ring rollback that changes nothing (one tiny kernel);
+    ``one_tile``: draft attention over a 64-slot ring (one 64-key tile per
+    (sequence, KV head), one split: the attention kernel alone);
+    ``one_tile_fused_step``: the fused draft step on that ring (attention, then
+    the merge that commits the append: the two launches of every draft step)."""
+    from speculative_decoding_attention_gb300 import wm
+
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    d = 8
+    gen = torch.Generator(device=device).manual_seed(77)
+    ring = wm.Ring.create(B, Hkv, D, 0, 64, device)
+    hist = torch.randn((B, Hkv, 64, D), generator=gen, device=device).to(torch.bfloat16)
+    wm.ring_fill(ring, wm.KVCache(hist, hist, torch.full((B,), 64, dtype=torch.int64, device=device)))
+    q = torch.randn((B, Hq, D), generator=gen, device=device).to(torch.bfloat16)
+    kn = torch.randn((B, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    keep = torch.full((B,), 64, dtype=torch.int64, device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
+    ws = wm.step_workspace(ring, Hq, n_split=1)
+    chains = {
+        "empty_kernel": lambda: [wm.ring_rollback(ring, keep) for _ in range(d)],
+        "one_tile": lambda: [wm.draft_attn(ring, q, w.scale, n_split=1, out=out, lse=lse) for _ in range(d)],
+        "one_tile_fused_step": lambda: ([wm.draft_step(ring, kn, kn, q, w.scale, ws, n_split=1, out=out, lse=lse)
+                                         for _ in range(d)], wm.ring_rollback(ring, keep)),
+    }
+    res = {}
+    for name, fn in chains.items():
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        ms = time_graph(g, flush, max(3, args.warmup), args.steps)
+        res[name] = round(1e3 * sum(ms) / len(ms) / d, 2)
+    res["note"] = (f"per launch (per draft step for the fused step), graphs of {d} dependent launches "
+                   f"with the workload's batch {B}, KV heads {Hkv}, head_dim {D} and {Hq // Hkv} rows per KV head")
+    return res
 
 
 def gpu_arm(args, rank, world, local):
@@ -381,7 +604,7 @@ def gpu_arm(args, rank, world, local):
     if wm.get_device_error():
         raise RuntimeError("device error during warm-up")
 
-    step_ms, draft_ms, verify_ms = [], [], []
+    step_ms = []
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
 
@@ -393,7 +616,7 @@ def gpu_arm(args, rank, world, local):
         clk.load_until_sampled(untimed_step, 3)
         barrier(world)
         torch.cuda.synchronize()
-        t_begin = time.time()
+        t_begin = time.monotonic()
         for _ in range(args.steps):
             flush()
             e0.record()
@@ -402,21 +625,12 @@ def gpu_arm(args, rank, world, local):
             e1.synchronize()
             step_ms.append(e0.elapsed_time(e1))
         torch.cuda.synchronize()
-        t_end = time.time()
+        t_end = time.monotonic()
         barrier(world)
         clk.mark(t_begin, t_end)
         clk.load_until_sampled(untimed_step, 2)
     clocks = clk.summary()
-    # Breakdown: the step captured with in-graph events, replayed the same way.
-    st.capture(events=True)
-    if st.ev:
-        for i in range(max(3, args.warmup) + args.steps):
-            flush()
-            st.graph.replay()
-            torch.cuda.synchronize()
-            if i >= max(3, args.warmup):
-                draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
-                verify_ms.append(st.ev[1].elapsed_time(st.ev[2]))
+    draft_ms, verify_ms = breakdown(st, flush, args)
     # The same step graph replayed without the flush: the ring stays in L2
     # from one step to the next (the verify streams its cache evict-first).
     warm_draft_ms = []
@@ -427,13 +641,15 @@ def gpu_arm(args, rank, world, local):
             if i >= 3:
                 warm_draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
     if not st.ev:  # no in-graph events: time the verify alone, same way
+        vms = []
         for _ in range(args.steps):
             flush()
             e0.record()
             wm.verify_attn(st.kv, st.inp.q_verify, w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
             e1.record()
             e1.synchronize()
-            verify_ms.append(e0.elapsed_time(e1))
+            vms.append(e0.elapsed_time(e1))
+        verify_ms = sum(vms) / len(vms)
     if wm.get_device_error():
         raise RuntimeError("device error during the timed steps")
     out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
@@ -442,13 +658,12 @@ def gpu_arm(args, rank, world, local):
     masw = masw_draft_chain(st, flush, args)
 
     us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
-    us_verify = 1e3 * sum(verify_ms) / len(verify_ms)
-    us_draft = 1e3 * sum(draft_ms) / len(draft_ms) if draft_ms else None
+    us_verify = 1e3 * verify_ms
+    us_draft = 1e3 * draft_ms if draft_ms else None
 
     B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
     sum_n = sum(st.inp.seq_lens_host)
-    verify_bytes = 2 * Hkv * D * 2 * sum_n + 2 * (B * st.T * Hq * D * 2) + B * st.T * Hq * 4
-    draft_bytes = 2 * B * Hkv * w.slots * D * 2 + 2 * (B * Hq * D * 2) + B * Hq * 4
+    verify_bytes, draft_bytes = step_bytes(st)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
@@ -457,12 +672,24 @@ def gpu_arm(args, rank, world, local):
     draft_gbs = draft_bytes * depth / (us_draft * 1e-6) / 1e9 if us_draft else None
 
     e2e = None if args.no_e2e else e2e_leg(st, args, world, device)
+    floors = None if args.context else launch_floors(w, device, flush, args)
+    # the other 1M-context configurations (the headline stays the default workload)
+    others = {}
+    if args.workload == workloads.BENCH_WORKLOAD and depth == workloads.BENCH_DEPTH and not args.context \
+            and not args.no_extra:
+        launches_before = st.launches_per_step()
+        for name, dd in (("hybrid_1m_d256", 1), ("hybrid_1m_d256", 5), ("nope_1m_b2", 4)):
+            others[f"{name}/d{dd}"] = extra_1m_line(name, dd, device, flush, args, peak)
+        assert launches_before == st.launches_per_step()
     cpu = None
     if not args.no_cpu and rank == 0:
         cpu = cpu_baseline(st, args)
 
     if rank != 0:
         return
+    config = workload_config(w, depth, args.context, world)
+    if w.ragged:
+        config["context_per_sequence"] = list(st.inp.seq_lens_host)
     line = {
         "metric": METRIC,
         "value": round(us_step, 2),
@@ -476,21 +703,13 @@ def gpu_arm(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
-        "config": {
-            "workload": w.name,
-            "batch": B, "context": (args.context if args.context else w.context) if not w.ragged else
-            list(st.inp.seq_lens_host),
-            "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": D, "sink": w.sink, "window": w.window,
-            "draft_depth": depth, "verify_positions": st.T, "kv_layout": "paged" if w.page_size else "contiguous",
-            "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+        "config": config,
+        "detail": {
+            "execution": "one CUDA graph per step holding the step's kernels only; the draft / verify breakdown "
+                         "comes from a second capture with events between them",
             "draft_execution": "per draft step: one launch of ring append fused into the draft attention, "
                                "then the split merge (which commits the append)",
-            "l2": "flushed between timed steps (write of a 2x L2 buffer, then a read of another 2x L2 buffer so "
-                  "the flush's dirty lines are written back before the step); each step also reads the full "
-                  "KV cache (> L2)",
-            "execution": "one CUDA graph per step (kernels only; the draft / verify breakdown in detail comes from a second capture with events between them)", "parallelism": f"replicas x{world}",
-        },
-        "detail": {
+            "draft_splits": st.d_splits, "verify_splits": st.v_splits,
             "step_us_median": round(1e3 * sorted(step_ms)[len(step_ms) // 2], 2),
             "verify_us": round(us_verify, 2),
             "verify_gbs": round(achieved, 1),
@@ -505,6 +724,7 @@ def gpu_arm(args, rank, world, local):
                                           if warm_draft_ms else None),
             "draft_warm_l2": "the same step graph replayed without the flush: the ring stays in L2 from step "
                              "to step (the verify reads its cache evict-first)",
+            "draft_launch_floor_us": floors,
             "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
             "masw_draft": masw,
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
@@ -514,6 +734,7 @@ def gpu_arm(args, rank, world, local):
             "native_draft_us_per_step": round(1e3 * native_ms / depth, 2),
             "native_step_us": round(1e3 * native_step_ms, 2),
             "native_over_windowed_step": round(1e3 * native_step_ms / us_step, 3),
+            "other_1m_configs": others or None,
         },
         "roofline": {
             "kernel": "attn_tc_kernel (tcgen05 verify, split-KV) + lse_merge",
@@ -730,31 +951,25 @@ def e2e_leg(st: Step, args, world, device) -> dict:
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, depth, inp_host, rows_fraction):
-    """One bounded sample of the step on the host: every draft row of the d
-    draft steps, and an evenly spaced fraction of the verify rows.  Returns
-    (seconds spent, seconds per whole step, description, seconds per draft
-    step, seconds per whole verify)."""
+def oracle_step(w, depth, inp_host) -> tuple[float, float]:
+    """One whole step on the host cores: every row of the d draft steps and
+    every verify row, as the GPU computes them.  Returns (seconds of the draft
+    steps, seconds of the verify)."""
     import oracle
 
-    B, Hq, T = w.batch, w.n_q_heads, depth + 1
     hist = oracle.KV(inp_host["k"], inp_host["v"], inp_host["block_table"])
     t0 = time.perf_counter()
     for j in range(depth):
         pos = [n + j for n in inp_host["lens"]]
         oracle.draft(hist, inp_host["q_draft"][j], pos, w.sink, w.window, w.scale)
-    t_draft = time.perf_counter() - t0
-    total_rows = B * T * Hq
-    n_rows = max(1, int(round(total_rows * rows_fraction)))
-    rows = [int(round(i * total_rows / n_rows)) for i in range(n_rows)]
     t1 = time.perf_counter()
-    oracle.verify(hist, inp_host["q_verify"], inp_host["lens"], w.scale, rows=rows)
-    t_verify = time.perf_counter() - t1
-    verify_s = t_verify * total_rows / n_rows
-    per_step = t_draft + verify_s
-    desc = (f"all {B * Hq} draft rows x {depth} draft steps + {n_rows}/{total_rows} verify rows "
-            f"(scaled x{total_rows / n_rows:.2f}) of {w.name}")
-    return t_draft + t_verify, per_step, desc, t_draft / max(1, depth), verify_s
+    oracle.verify(hist, inp_host["q_verify"], inp_host["lens"], w.scale)
+    return t1 - t0, time.perf_counter() - t1
+
+
+def step_description(w, depth) -> str:
+    return (f"whole steps: all {w.batch * w.n_q_heads} draft rows x {depth} draft steps + all "
+            f"{w.batch * (depth + 1) * w.n_q_heads} verify rows of {w.name}")
 
 
 def host_inputs(inp):
@@ -763,39 +978,32 @@ def host_inputs(inp):
             "lens": list(inp.seq_lens_host), "q_draft": inp.q_draft.cpu(), "q_verify": inp.q_verify.cpu()}
 
 
-def pick_fraction(w, depth, inp_host, budget_s):
-    """Verify-row fraction whose oracle time is about ``budget_s`` seconds."""
-    probe = 1.0 / (w.batch * (depth + 1) * w.n_q_heads)
-    secs = oracle_sample(w, depth, inp_host, probe)[0]
-    rows_per_s = 1.0 / max(secs, 1e-6)
-    frac = min(1.0, budget_s * rows_per_s / (w.batch * (depth + 1) * w.n_q_heads))
-    return max(probe, frac)
-
-
 def cpu_baseline(st: Step, args, min_seconds: float = 10.0) -> dict:
-    """The oracle timed on repeated bounded samples until about ``min_seconds``
-    of CPU work have run; reported per whole step."""
+    """The oracle timed on whole steps of the workload (no sampling of rows,
+    nothing scaled) until about ``min_seconds`` of CPU work have run."""
     import oracle
 
     oracle.set_num_threads(len(os.sched_getaffinity(0)))  # every host core this process may use
     inp_host = host_inputs(st.inp)
-    frac = pick_fraction(st.w, st.d, inp_host, budget_s=min_seconds / 2)
-    total, per_steps, drafts, verifies, desc = 0.0, [], [], [], ""
-    while total < min_seconds:
-        secs, per_step, desc, draft_s, verify_s = oracle_sample(st.w, st.d, inp_host, frac)
-        total += secs
-        per_steps.append(per_step)
-        drafts.append(draft_s)
-        verifies.append(verify_s)
-    n = len(per_steps)
-    return {"value": round(1e6 * sum(per_steps) / n, 1), "unit": UNIT,
+    oracle_step(st.w, st.d, inp_host)  # warm-up: page faults, thread pool
+    drafts, verifies = [], []
+    while sum(drafts) + sum(verifies) < min_seconds or not drafts:
+        dr, ve = oracle_step(st.w, st.d, inp_host)
+        drafts.append(dr)
+        verifies.append(ve)
+    n = len(drafts)
+    per_step = (sum(drafts) + sum(verifies)) / n
+    return {"value": round(1e6 * per_step, 1), "unit": UNIT,
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} x ({desc})", "sample_seconds": round(total, 2),
-            "draft_us_per_step": round(1e6 * sum(drafts) / n, 1), "verify_us": round(1e6 * sum(verifies) / n, 1)}
+            "sample": f"{n} {step_description(st.w, st.d)} (1 untimed)",
+            "sample_seconds": round(sum(drafts) + sum(verifies), 2),
+            "draft_us_per_step": round(1e6 * sum(drafts) / n / st.d, 1),
+            "verify_us": round(1e6 * sum(verifies) / n, 1)}
 
 
 def reference_arm(args, rank, world, local):
-    """The fp64 CPU oracle on the host cores, on the GPU arm's workload."""
+    """The fp64 CPU oracle on the host cores, on the GPU arm's workload: each
+    warm-up and timed step is one whole step (every draft and verify row)."""
     import oracle
 
     if world > 1:
@@ -811,31 +1019,33 @@ def reference_arm(args, rank, world, local):
     depth = args.depth if args.depth is not None else (
         workloads.BENCH_DEPTH if args.workload == workloads.BENCH_WORKLOAD else w.max_depth)
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = wm_inputs.make_inputs(w, depth=depth, device=gen_dev)
+    inp = wm_inputs.make_inputs(w, depth=depth, device=gen_dev, context=args.context)
     inp_host = host_inputs(inp)
+    lens = list(inp.seq_lens_host)
     del inp
-    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
-    frac = pick_fraction(w, depth, inp_host, budget_s=budget)
     for _ in range(args.warmup):
-        oracle_sample(w, depth, inp_host, frac)
-    per_steps, drafts, verifies, secs_total, desc = [], [], [], 0.0, ""
+        oracle_step(w, depth, inp_host)
+    drafts, verifies = [], []
     for _ in range(args.steps):
-        secs, per_step, desc, draft_s, verify_s = oracle_sample(w, depth, inp_host, frac)
-        per_steps.append(per_step)
-        drafts.append(draft_s)
-        verifies.append(verify_s)
-        secs_total += secs
-    us = 1e6 * sum(per_steps) / len(per_steps)
+        dr, ve = oracle_step(w, depth, inp_host)
+        drafts.append(dr)
+        verifies.append(ve)
+    us = 1e6 * (sum(drafts) + sum(verifies)) / args.steps
+    config = workload_config(w, depth, args.context, world)
+    if w.ragged:
+        config["context_per_sequence"] = lens
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
-        "config": {"workload": w.name, "draft_depth": depth, "verify_positions": depth + 1,
-                   "parallelism": "host cores (OpenMP over rows)"},
+        "config": config,
+        "detail": {"execution": "the fp64 oracle (plain C, OpenMP over rows) on the host cores, one whole step "
+                                "per timed step"},
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": desc, "draft_us_per_step": round(1e6 * sum(drafts) / len(drafts), 1),
-                         "verify_us": round(1e6 * sum(verifies) / len(verifies), 1)},
+                         "sample": f"{args.steps} {step_description(w, depth)}",
+                         "draft_us_per_step": round(1e6 * sum(drafts) / args.steps / depth, 1),
+                         "verify_us": round(1e6 * sum(verifies) / args.steps, 1)},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

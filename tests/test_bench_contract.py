@@ -35,7 +35,12 @@ def test_reference_arm_prints_one_contract_line():
     assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["higher_is_better"] is False and d["value"] > 0
     assert d["config"]["workload"] == "tiny_4k"
+    bench = load_bench()
+    from speculative_decoding_attention_gb300 import workloads
+    # the same config keys and values as the GPU arm reports for this workload
+    assert d["config"] == bench.workload_config(workloads.get("tiny_4k"), 1, None, 1)
     cb = d["cpu_baseline"]
+    assert cb["sample"].startswith("3 whole steps")
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
@@ -53,10 +58,10 @@ def test_clock_summary_counts_samples_in_the_timed_region(tmp_path):
     clk = bench.ClockSampler(torch.device("cpu"))
     clk.path = str(tmp_path / "clocks.csv")
     clk.interval_ms = 20
-    t0 = time.time()
+    t0, m0 = time.time(), time.monotonic()
     quiet = (False, False, False, False)
     write_samples(clk.path, t0, [(2070, quiet)] * 3 + [(2055, quiet)] * 4 + [(2070, quiet)] * 2)
-    clk.mark(t0 + 0.05, t0 + 0.13)  # samples 3..6
+    clk.mark(m0 + 0.05, m0 + 0.13)  # samples 3..6 (the summary maps the wall-clock stamps to monotonic time)
     s = clk.summary()
     assert s["samples"] == 9 and s["samples_in_timed_region"] == 4
     assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070 and s["reasons"] == []
@@ -113,3 +118,23 @@ def test_packed_buffers_are_aligned_views():
     # the views do not overlap and stay inside the buffer
     ends = sorted((t.data_ptr() - base, t.data_ptr() - base + t.numel() * t.element_size()) for t in views.values())
     assert all(a[1] <= b[0] for a, b in zip(ends, ends[1:])) and ends[-1][1] <= buf.numel()
+
+
+def test_nvml_samples_and_reason_bits(tmp_path):
+    """The NVML sampler's rows: monotonic time, SM MHz, max MHz, reason bits."""
+    bench = load_bench()
+    clk = bench.ClockSampler(torch.device("cpu"))
+    clk.path = str(tmp_path / "nvml.csv")
+    clk.source, clk.interval_ms = "nvml", 0.5
+    m0 = time.monotonic()
+    rows = [(m0 + 0.0005 * k, 2070, 2070, 0) for k in range(20)]
+    rows[7] = (rows[7][0], 1950, 2070, 0x4)      # sw_power_cap
+    rows[15] = (rows[15][0], 1500, 2070, 0x8 | 0x40)  # hw_slowdown, hw_thermal_slowdown
+    with open(clk.path, "w") as f:
+        for r in rows:
+            f.write(f"{r[0]:.6f},{r[1]},{r[2]},{r[3]}\n")
+    clk.mark(m0 + 0.0026, m0 + 0.0061)  # samples 6..12
+    s = clk.summary()
+    assert s["samples"] == 20 and s["samples_in_timed_region"] == 7 and s["source"] == "nvml"
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    assert s["sm_mhz"] == 2070 and s["sm_mhz_timed_region"] == 2070
