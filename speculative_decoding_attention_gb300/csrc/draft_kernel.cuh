@@ -30,7 +30,9 @@
 // At the end the four warps' states meet once in shared memory (the staging
 // area, free by then): row maxima, sums and O^T, combined in a fixed order.
 // The split's normalised output and log-sum-exp go to the bf16 output (one
-// split) or to fp32 partials that the merge kernel combines.
+// split) or to fp32 partials that the merge kernel combines.  Splits are
+// balanced: split s of n takes key tiles s*T/n .. (s+1)*T/n - 1 of the T tiles,
+// so every planned count is realised with at most one tile of difference.
 //
 // P goes into the P.V product as two bf16 parts, hi = bf16(p) and
 // lo = bf16(p - hi), so the weights keep ~2^-17 relative accuracy.
@@ -135,8 +137,9 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
         }
         n_keys = p.mem_base + mc;
     }
-    const int64_t k_begin = (int64_t)split * p.keys_per_split;
-    const int64_t k_end = min(k_begin + (int64_t)p.keys_per_split, n_keys);
+    // balanced splits: split s takes tiles s * T / n .. (s + 1) * T / n - 1
+    const int64_t k_begin = (int64_t)split * p.plan_tiles / p.n_split * TK;
+    const int64_t k_end = min((int64_t)(split + 1) * p.plan_tiles / p.n_split * TK, n_keys);
     const int n_tiles = k_end > k_begin ? (int)((k_end - k_begin + TK - 1) / TK) : 0;
     const int64_t mem_lo = p.mem_count ? p.mem_base : INT64_MAX;
 
@@ -203,15 +206,20 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
 
     // Prologue: every load first (n_seen, the first tile's tags, Q^T fragments,
     // the appended rows), then the stores, so their latencies overlap each
-    // other and the first tile's copy.
-    const int32_t *tags = p.pos_tag + (int64_t)b * p.n_slots;
-    const int64_t ring_end = min(k_end, (int64_t)p.n_slots);  // memory slots carry no tag
+    // other and the first tile's copy.  Inside the split, key indices are
+    // 32-bit offsets from k_begin (a split never exceeds the ring plus the
+    // memory store, both bounded by INT32_MAX / 2).
+    const int32_t klen = (int32_t)(k_end - k_begin);                                   // keys of the split
+    const int32_t ring_rel = (int32_t)max((int64_t)0, min(k_end, (int64_t)p.n_slots) - k_begin);  // tagged keys
+    const int32_t mem_rel = k_end > mem_lo ? (int32_t)(mem_lo - k_begin) : INT32_MAX;  // first memory key
+    const int32_t *tags = p.pos_tag + (int64_t)b * p.n_slots + k_begin;
     int64_t seen = p.n_seen[b];
     // this thread's keys in a tile: key g and key g + 8 of its warp's 16
+    const int32_t kw_lane = C::KW * warp + g;
     auto load_tags = [&](int t, int32_t &t0, int32_t &t1) {
-        const int64_t ka = k_begin + (int64_t)t * TK + C::KW * warp + g;
-        t0 = ka < ring_end ? __ldg(tags + ka) : -1;
-        t1 = ka + 8 < ring_end ? __ldg(tags + ka + 8) : -1;
+        const int32_t ka = t * TK + kw_lane;
+        t0 = ka < ring_rel ? __ldg(tags + ka) : -1;
+        t1 = ka + 8 < ring_rel ? __ldg(tags + ka + 8) : -1;
     };
     int32_t tg0 = -1, tg1 = -1;
     if (n_tiles > 0) load_tags(0, tg0, tg1);
@@ -250,15 +258,30 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     const int64_t new_slot =
         (STEP && seen >= 0) ? (seen < p.sink ? seen : p.sink + (seen - p.sink) % p.window) : -1;
     const bool has_new = STEP && new_slot >= k_begin && new_slot < k_end;
+    // The key set in 32-bit terms.  Tags are int32 (a ring never holds a
+    // position >= INT32_MAX), so clamping the query position and the window's
+    // lower edge into int32 keeps every comparison exact.
+    const int32_t qp = (int32_t)min(qpos, (int64_t)INT32_MAX);
+    const int32_t lo = (int32_t)max(min(qpos - p.window, (int64_t)INT32_MAX), (int64_t)INT32_MIN);
+    const int32_t sink = p.sink;
+    const int32_t new_rel = has_new ? (int32_t)(new_slot - k_begin) : -1;
+    auto tag_ok = [&](int32_t t) { return t >= 0 && t <= qp && (t < sink || t > lo); };
 
-    auto key_ok = [&](int64_t kabs, int32_t tag) -> bool {
-        if (kabs >= k_end) return false;
-        if (kabs >= mem_lo) return true;
-        const int64_t t = (STEP && kabs == new_slot) ? qpos : (int64_t)tag;
-        return t >= 0 && t <= qpos && (t < p.sink || t > qpos - p.window);
-    };
+    // ldmatrix row addresses (this lane's row of its 8x8 matrix) within a
+    // stage, for k-steps / head-dim blocks 0..3 of each 64-column chunk; the
+    // chunk adds a constant TK * 128 bytes.  Rows are 16w + (0 or 8) + lr, so
+    // a row's 128-byte swizzle phase is lr.
+    uint32_t koff[4], voff[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int krow = C::KW * warp + (lm & 1) * 8 + lr;  // S^T: A = K[16 keys x 16 dims]
+        koff[c] = krow * 128 + ((((2 * c + (lm >> 1)) & 7) ^ lr) << 4);
+        const int vrow = C::KW * warp + (lm >> 1) * 8 + lr;  // O^T: A = V^T[16 dims x 16 keys] (transposed load)
+        voff[c] = vrow * 128 + ((((2 * c + (lm & 1)) & 7) ^ lr) << 4);
+    }
 
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows 2*t4 and 2*t4 + 1
+    float m_use[2] = {0.f, 0.f};                      // m_run, or 0 while it is -inf
     float l_run[2] = {0.f, 0.f};                      // this thread's keys only
     float oacc[C::KSTEPS][4];
 #pragma unroll
@@ -271,19 +294,20 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
         const int s = t % C::STAGES;
         int32_t nt0 = -1, nt1 = -1;
         if (t + 1 < n_tiles) load_tags(t + 1, nt0, nt1);
-        if (!*abort_flag && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
+        bool live = !*abort_flag;
+        if (live && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
             draft_report(p.err, WM_DEVERR_TIMEOUT);
             *abort_flag = 1;
+            live = false;
         }
-        const bool live = !*abort_flag;
-        const int64_t kw0 = k_begin + (int64_t)t * TK + C::KW * warp;  // this warp's first key
+        const int32_t kt = t * TK;  // the tile's first key, relative to the split
         const uint32_t sK = sbase + s * C::STAGE_BYTES;
         const uint32_t sV = sK + C::TILE_BYTES;
         bool wrote_smem = false;
         if (live) {
             // ---- STEP: the appended rows replace the ring's stale row in the staged tile
-            if (has_new && new_slot >= kw0 && new_slot < kw0 + C::KW) {
-                const int row = C::KW * warp + (int)(new_slot - kw0);
+            if (STEP && new_rel >= kt + C::KW * warp && new_rel < kt + C::KW * warp + C::KW) {
+                const int row = new_rel - kt;
 #pragma unroll
                 for (int j = 0; j < VPL; ++j) {
                     const int i = lane + 32 * j;
@@ -301,19 +325,26 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
                 uint32_t a[4];
-                const int key = C::KW * warp + (lm & 1) * 8 + lr;
-                const int d = kk * 16 + (lm >> 1) * 8;
-                ldsm_x4(sK + (d >> 6) * (TK * 128) + swz128(key, (d & 63) >> 3), a[0], a[1], a[2], a[3]);
+                ldsm_x4(sK + koff[kk & 3] + (kk >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
                 mma_bf16((kk & 1) ? sb : sa, a, qf[kk][0], qf[kk][1]);
+            }
+            // masks of this thread's two keys: memory tiles hold only keys; ring
+            // keys are judged by their tags (the appended slot holds qpos)
+            const int32_t k0 = kt + kw_lane, k1 = k0 + 8;
+            bool ok0, ok1;
+            if (kt >= mem_rel) {
+                ok0 = k0 < klen;
+                ok1 = k1 < klen;
+            } else {
+                ok0 = k0 < klen && tag_ok(STEP && k0 == new_rel ? qp : tg0);
+                ok1 = k1 < klen && tag_ok(STEP && k1 == new_rel ? qp : tg1);
             }
             // sv[0], sv[1]: key g, rows 2t4 and 2t4+1; sv[2], sv[3]: key g + 8
             float sv[4];
-            const bool ok0 = key_ok(kw0 + g, tg0), ok1 = key_ok(kw0 + g + 8, tg1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sv[e] = (sa[e] + sb[e]) * p.scale_log2;
-                if (!(e < 2 ? ok0 : ok1)) sv[e] = -CUDART_INF_F;
-            }
+            sv[0] = ok0 ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+            sv[1] = ok0 ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+            sv[2] = ok1 ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+            sv[3] = ok1 ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
             // ---- tile max per row over the warp's 16 keys
             float tmax[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
 #pragma unroll
@@ -332,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
                     const float mn = rz[h] ? tmax[h] : m_run[h];
                     alpha[h] = rz[h] ? ex2(m_run[h] - mn) : 1.f;  // 0 when m_run was -inf
                     m_run[h] = mn;
+                    m_use[h] = mn == -CUDART_INF_F ? 0.f : mn;
                     l_run[h] *= alpha[h];
                 }
 #pragma unroll
@@ -342,10 +374,8 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
                     oacc[i][3] *= alpha[1];
                 }
             }
-            const float mu0 = m_run[0] == -CUDART_INF_F ? 0.f : m_run[0];
-            const float mu1 = m_run[1] == -CUDART_INF_F ? 0.f : m_run[1];
-            const float p0 = ex2(sv[0] - mu0), p1 = ex2(sv[1] - mu1);
-            const float p2 = ex2(sv[2] - mu0), p3 = ex2(sv[3] - mu1);
+            const float p0 = ex2(sv[0] - m_use[0]), p1 = ex2(sv[1] - m_use[1]);
+            const float p2 = ex2(sv[2] - m_use[0]), p3 = ex2(sv[3] - m_use[1]);
             l_run[0] += p0 + p2;
             l_run[1] += p1 + p3;
             // ---- P^T as the B operand: hi and lo bf16 parts, transposed in registers
@@ -356,29 +386,34 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
             const uint32_t l23 = pack_bf16(p2 - __low2float(hb23), p3 - __high2float(hb23));
             const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
             const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
-            // ---- keys masked for every row: their V^T operand elements are zeroed
+            // ---- keys masked for every row: their V^T operand elements are
+            // zeroed (only on tiles that have such keys)
             const uint32_t okb0 = __ballot_sync(0xffffffffu, ok0), okb1 = __ballot_sync(0xffffffffu, ok1);
-            const bool all_ok = (okb0 & okb1) == 0xffffffffu;
-            // this thread's V^T columns are keys 2t4, 2t4+1 (a0, a1) and 2t4+8, 2t4+9 (a2, a3)
-            const uint32_t mlo = (((okb0 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
-                                 (((okb0 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
-            const uint32_t mhi = (((okb1 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
-                                 (((okb1 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
-            // ---- O^T += V^T P^T over the whole head dim
+            if ((okb0 & okb1) == 0xffffffffu) {
 #pragma unroll
-            for (int i = 0; i < C::KSTEPS; ++i) {
-                uint32_t a[4];
-                const int key = C::KW * warp + (lm >> 1) * 8 + lr;
-                const int d = i * 16 + (lm & 1) * 8;
-                ldsm_x4_t(sV + (d >> 6) * (TK * 128) + swz128(key, (d & 63) >> 3), a[0], a[1], a[2], a[3]);
-                if (!all_ok) {
+                for (int i = 0; i < C::KSTEPS; ++i) {
+                    uint32_t a[4];
+                    ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
+                    mma_bf16(oacc[i], a, bh0, bh1);
+                    mma_bf16(oacc[i], a, bl0, bl1);
+                }
+            } else {
+                // this thread's V^T columns: keys 2t4, 2t4+1 (a0, a1) and 2t4+8, 2t4+9 (a2, a3)
+                const uint32_t mlo = (((okb0 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                     (((okb0 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
+                const uint32_t mhi = (((okb1 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                     (((okb1 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int i = 0; i < C::KSTEPS; ++i) {
+                    uint32_t a[4];
+                    ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
                     a[0] &= mlo;
                     a[1] &= mlo;
                     a[2] &= mhi;
                     a[3] &= mhi;
+                    mma_bf16(oacc[i], a, bh0, bh1);
+                    mma_bf16(oacc[i], a, bl0, bl1);
                 }
-                mma_bf16(oacc[i], a, bh0, bh1);
-                mma_bf16(oacc[i], a, bl0, bl1);
             }
         }
         if (wrote_smem) fence_proxy_async_smem();  // the stage is refilled by TMA later
@@ -419,11 +454,12 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
         red_l[warp * kDraftRows + 2 * t4] = l_run[0];
         red_l[warp * kDraftRows + 2 * t4 + 1] = l_run[1];
     }
-    // after an aborted pipeline copies may still land in the staging area:
-    // outputs are then not written (the decision is the same in every warp)
-    if (named_bar_sync_or(1, NCT, *abort_flag != 0)) return;
+    // After an aborted pipeline, copies may still land in the staging area:
+    // this CTA's result is then not written (the decision is the same in
+    // every warp).
+    const bool aborted = named_bar_sync_or(1, NCT, *abort_flag != 0);
     float *obuf = reinterpret_cast<float *>(gbase);  // the staging area: every copy has landed and been read
-    {
+    if (!aborted) {
         float f[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -445,7 +481,9 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     }
     named_bar_sync(1, NCT);
 
-    // ---- normalise and write: 16 threads per row, float4 columns (c, c + 64, ...)
+    // ---- this split's result: 16 threads per row, float4 columns (c, c + 64, ...);
+    // the final output when unsplit, else fp32 partials for the merge kernel
+    if (aborted) return;
     const float kLn2 = 0.693147180559945309f;
     const int tid = threadIdx.x;
     const int r = tid >> 4;  // row 0..7

@@ -126,7 +126,8 @@ bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 struct SplitPlan {
     int n_split = 0;
-    int keys_per_split = 0;
+    int keys_per_split = 0;  // uniform splits: keys per split (the last one may be shorter)
+    int plan_tiles = 0;      // balanced splits (keys-as-M draft kernel): tiles shared out as evenly as possible
 };
 
 // Which attention kernel serves a call.  Verification at head dim 128/256 runs
@@ -192,7 +193,13 @@ int ctas_per_sm(int op, int head_dim, int rows) {
 // more than one wave, the count is raised to fill the last wave (the most
 // splits that still take that many waves): with equal lengths a partly empty
 // last wave would leave SMs idle for a whole split's time.
-SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim, int per_sm) {
+// Balanced (the keys-as-M draft kernel): split s takes key tiles
+// floor(s * tiles / n) .. floor((s + 1) * tiles / n) - 1, so any split count up
+// to the tile count is used as planned -- uniform splits
+// of whole tiles can only realise the counts that divide the tiles evenly,
+// which left a third of the SMs with one CTA less than the others.
+SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int tile, int head_dim, int per_sm,
+                      bool balanced = false) {
     SplitPlan pl;
     const int64_t tiles = std::max<int64_t>(1, (max_keys + tile - 1) / tile);
     int64_t ns = requested;
@@ -212,6 +219,12 @@ SplitPlan plan_splits(int units, int batch, int64_t max_keys, int requested, int
     }
     ns = std::min<int64_t>(ns, tiles);
     const int64_t tps = (tiles + ns - 1) / ns;
+    if (balanced) {
+        pl.n_split = (int)ns;
+        pl.plan_tiles = (int)std::min<int64_t>(tiles, INT32_MAX);
+        pl.keys_per_split = (int)((tiles + ns - 1) / ns * tile);
+        return pl;
+    }
     pl.n_split = (int)((tiles + tps - 1) / tps);
     pl.keys_per_split = (int)(tps * tile);
     return pl;
@@ -333,8 +346,9 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
         if (n_q != 1) return 0;
         op = WM_OP_DRAFT;  // all draft forms split alike
     }
+    const int rows = n_q * (n_q_heads / n_kv_heads);
     return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim,
-                       ctas_per_sm(op, head_dim, n_q * (n_q_heads / n_kv_heads)))
+                       ctas_per_sm(op, head_dim, rows), use_draft_kernel(op, rows))
         .n_split;
 }
 
@@ -428,11 +442,13 @@ static wm_status run_attention(int op, AttnParams &p, const MapEncoder &encode_m
                                int64_t *commit_n_seen = nullptr) {
     const bool step = commit_n_seen != nullptr;
     if ((int64_t)p.batch * p.n_kv_heads > kMaxUnits) return WM_ERR_UNSUPPORTED;
+    const bool keys_as_m = use_draft_kernel(op, p.rows);
     const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim),
-                                     p.head_dim, ctas_per_sm(op, p.head_dim, p.rows));
+                                     p.head_dim, ctas_per_sm(op, p.head_dim, p.rows), keys_as_m);
     const int64_t rows_total = (int64_t)p.batch * p.n_q * p.n_q_heads;
     p.n_split = pl.n_split;
     p.keys_per_split = pl.keys_per_split;
+    p.plan_tiles = pl.plan_tiles;
     p.out = out;
     p.lse = lse;
     p.o_part = nullptr;

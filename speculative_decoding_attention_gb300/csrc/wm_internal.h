@@ -80,6 +80,9 @@ struct AttnParams {
     // copies, -1 for none
     uint32_t wait_limit;
     int32_t stall_tile;
+    // keys-as-M draft kernel only: balanced splits (split s covers key tiles
+    // s * plan_tiles / n_split .. (s + 1) * plan_tiles / n_split - 1)
+    int32_t plan_tiles;
 };
 
 // Launch the attention kernel for head dim D (defined in attn_d<D>.cu).  mk/mv

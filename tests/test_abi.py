@@ -193,6 +193,10 @@ def test_draft_step_workspace(lib):
         assert wm.workspace_size(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 1, D, 4100, ns) == \
             ((o + 255) // 256) * 256 + rows * ns * 4
     assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 1, 256, 4100, 1000) == 65  # one tile per split at most
+    # up to 8 query heads per KV head the draft splits are balanced (any count up
+    # to the tile count); more rows keep uniform splits of whole tiles
+    assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 1, 128, 4100, 30) == 30
+    assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 32, 1, 128, 4100, 30) == 22  # 3 tiles per split
     assert wm.plan_splits(wm.WM_OP_DRAFT_STEP, 1, 2, 16, 2, 256, 4100, 4) == 0      # one query position only
 
 
