@@ -31,8 +31,9 @@
 // area, free by then): row maxima, sums and O^T, combined in a fixed order.
 // The split's normalised output and log-sum-exp go to the bf16 output (one
 // split) or to fp32 partials that the merge kernel combines.  Splits are
-// balanced: split s of n takes key tiles s*T/n .. (s+1)*T/n - 1 of the T tiles,
-// so every planned count is realised with at most one tile of difference.
+// balanced: of T = q n + r key tiles, the first r of the n splits take q + 1
+// tiles and the others q, so every planned count is realised with at most one
+// tile of difference.
 //
 // P goes into the P.V product as two bf16 parts, hi = bf16(p) and
 // lo = bf16(p - hi), so the weights keep ~2^-17 relative accuracy.
@@ -123,6 +124,38 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     const int kvh = unit - b * p.n_kv_heads;
     const int split = blockIdx.x;
 
+    // ---- set-up that reads only kernel parameters and this CTA's shared
+    // memory runs before the wait on the previous kernel, while it drains:
+    // the split's planned key range, the pipeline barriers, the tensor-map
+    // prefetches and the L2 policy
+    // balanced splits: T = q n + r tiles; the first r splits take q + 1 tiles, the rest q
+    const int32_t tq = p.plan_tiles / p.n_split, tr = p.plan_tiles - tq * p.n_split;
+    const int32_t t_first = split * tq + min(split, tr);
+    const int64_t k_begin = (int64_t)t_first * TK;
+    const int64_t k_end_plan = (int64_t)(t_first + tq + (split < tr ? 1 : 0)) * TK;
+    const int64_t mem_lo = p.mem_count ? p.mem_base : INT64_MAX;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, C::NW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    uint64_t policy = 0;
+    if (warp == C::NW && lane == 0) {
+        if (k_begin < mem_lo) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+        if (k_end_plan > mem_lo) {
+            prefetch_tensormap(&tmk2);
+            prefetch_tensormap(&tmv2);
+        }
+        policy = l2_policy_evict_normal();  // the next draft step reads the ring again: normal L2 priority
+    }
+    __syncthreads();
+
     pdl_wait();  // every global read below may depend on the previous kernel
     pdl_launch_dependents();
 
@@ -137,35 +170,12 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
         }
         n_keys = p.mem_base + mc;
     }
-    // balanced splits: split s takes tiles s * T / n .. (s + 1) * T / n - 1
-    const int64_t k_begin = (int64_t)split * p.plan_tiles / p.n_split * TK;
-    const int64_t k_end = min((int64_t)(split + 1) * p.plan_tiles / p.n_split * TK, n_keys);
+    const int64_t k_end = min(k_end_plan, n_keys);
     const int n_tiles = k_end > k_begin ? (int)((k_end - k_begin + TK - 1) / TK) : 0;
-    const int64_t mem_lo = p.mem_count ? p.mem_base : INT64_MAX;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, C::NW);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
 
     // =========================================================== producer warp
     if (warp == C::NW) {
         if (lane == 0 && n_tiles > 0) {
-            if (k_begin < mem_lo) {
-                prefetch_tensormap(&tmk);
-                prefetch_tensormap(&tmv);
-            }
-            if (k_end > mem_lo) {
-                prefetch_tensormap(&tmk2);
-                prefetch_tensormap(&tmv2);
-            }
-            // the next draft step reads the ring again: normal L2 priority
-            const uint64_t policy = l2_policy_evict_normal();
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 if (t == p.stall_tile) break;  // tests of the timeout path only

@@ -193,8 +193,8 @@ int ctas_per_sm(int op, int head_dim, int rows) {
 // more than one wave, the count is raised to fill the last wave (the most
 // splits that still take that many waves): with equal lengths a partly empty
 // last wave would leave SMs idle for a whole split's time.
-// Balanced (the keys-as-M draft kernel): split s takes key tiles
-// floor(s * tiles / n) .. floor((s + 1) * tiles / n) - 1, so any split count up
+// Balanced (the keys-as-M draft kernel): with tiles = q n + r, the first r
+// splits take q + 1 tiles and the others q, so any split count up
 // to the tile count is used as planned -- uniform splits
 // of whole tiles can only realise the counts that divide the tiles evenly,
 // which left a third of the SMs with one CTA less than the others.

@@ -80,8 +80,8 @@ struct AttnParams {
     // copies, -1 for none
     uint32_t wait_limit;
     int32_t stall_tile;
-    // keys-as-M draft kernel only: balanced splits (split s covers key tiles
-    // s * plan_tiles / n_split .. (s + 1) * plan_tiles / n_split - 1)
+    // keys-as-M draft kernel only: balanced splits of the plan's key tiles
+    // (plan_tiles = q * n_split + r: the first r splits take q + 1 tiles, the rest q)
     int32_t plan_tiles;
 };
 
