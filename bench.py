@@ -527,7 +527,8 @@ def extra_1m_line(name: str, depth: int, device, flush, args, peak: float) -> di
                     "verify_frac_of_hbm": round(vg / peak, 4),
                     "draft_us_per_step": round(1e3 * draft_ms / depth, 2), "draft_gbs": round(dg, 1),
                     "draft_frac_of_hbm": round(dg / peak, 4), "draft_kv_bytes_per_step": db,
-                    "draft_splits": st.d_splits, "verify_splits": st.v_splits})
+                    "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+                    "draft_us_per_step_cuda_cores": fma_draft_chain(st, flush, args)})
     st.release()
     return out
 
@@ -656,6 +657,7 @@ def gpu_arm(args, rank, world, local):
     native_ms, native_step_ms = native_draft_chain(st, flush, args)
     unfused_ms = unfused_draft_chain(st, flush, args)
     masw = masw_draft_chain(st, flush, args)
+    fma_us = fma_draft_chain(st, flush, args)
 
     us_step = max_over_ranks(1e3 * sum(step_ms) / len(step_ms), world, device)
     us_verify = 1e3 * verify_ms
@@ -726,6 +728,9 @@ def gpu_arm(args, rank, world, local):
                              "to step (the verify reads its cache evict-first)",
             "draft_launch_floor_us": floors,
             "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
+            "draft_us_per_step_cuda_cores": fma_us,
+            "draft_cuda_cores": "the same fused draft chain with the draft kernel's Q.K and P.V on the CUDA cores "
+                                "(fp32 FMA, warp-shuffle softmax) instead of mma.sync, for comparison",
             "masw_draft": masw,
             "verify_kv_bytes": 2 * Hkv * D * 2 * sum_n,
             "outputs_finite": out_ok,
@@ -752,6 +757,44 @@ def gpu_arm(args, rank, world, local):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def fma_draft_chain(st: Step, flush, args):
+    """The fused draft chain with the draft kernel's products on the CUDA cores
+    (fp32 FMA, warp-shuffle softmax) instead of mma.sync: the measurement behind
+    the choice of tensor cores for the draft.  Mean us per draft step (in-graph
+    events around the chain, L2 flushed before each replay), or None without
+    in-graph events."""
+    wm, w, inp = st.wm, st.w, st.inp
+    wm.set_draft_math(wm.WM_DRAFT_MATH_FMA)
+    try:
+        ws = wm.step_workspace(st.ring, w.n_q_heads)
+
+        def chain(ev=None):
+            if ev:
+                ev[0].record()
+            for j in range(st.d):
+                wm.draft_step(st.ring, inp.k_new[j], inp.v_new[j], inp.q_draft[j], w.scale, ws, out=st.d_out[j],
+                              lse=st.d_lse[j])
+            if ev:
+                ev[1].record()
+            wm.ring_rollback(st.ring, st.base_len)
+
+        chain()
+        torch.cuda.synchronize()
+        try:
+            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        except TypeError:
+            return None
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=st.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            chain(ev)
+        ms = time_graph(g, flush, max(3, args.warmup), max(3, args.steps // 2), ev=ev)
+    finally:
+        wm.set_draft_math(wm.WM_DRAFT_MATH_MMA)
+    return round(1e3 * sum(m[0] for m in ms) / len(ms) / st.d, 2)
 
 
 def unfused_draft_chain(st: Step, flush, args):

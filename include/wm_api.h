@@ -360,6 +360,23 @@ const char *wm_status_string(wm_status status);
 int32_t wm_version(void);
 
 /*
+ * Arithmetic of the draft attention kernel for the draft calls made by the
+ * calling host thread (wm_draft_attn, wm_draft_attn_mem, wm_draft_step and
+ * wm_draft_attn_static with at most 8 query heads per KV head; no counterpart
+ * on the pages).  WM_DRAFT_MATH_MMA (the default): the Q.K^T and P.V products
+ * on the tensor cores with mma.sync, keys as the M dimension.
+ * WM_DRAFT_MATH_FMA: the same kernel with both products as fp32 FMA on the
+ * CUDA cores and the softmax maxima reduced with warp shuffles; the same
+ * results within the parity tolerance, kept to measure the choice between
+ * the two.  The split plan is queried per setting (wm_plan_splits and
+ * wm_workspace_size answer for the calling thread's setting).  Returns
+ * WM_ERR_INVALID_ARG for any other value.
+ */
+#define WM_DRAFT_MATH_MMA 0
+#define WM_DRAFT_MATH_FMA 1
+wm_status wm_set_draft_math(int32_t math);
+
+/*
  * Test support for the pipeline-wait timeout path (no counterpart on the
  * pages).  Every wait inside the attention kernels is bounded: after a limit
  * of polls the kernel records WM_DEVERR_TIMEOUT in the device error word,

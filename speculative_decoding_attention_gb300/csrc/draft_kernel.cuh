@@ -65,7 +65,9 @@ namespace wm {
 // Rows (query heads per KV head) the keys-as-M draft kernel serves: the N of its mma.
 constexpr int kDraftRows = kDraftRowsMax;
 
-template <int D>
+// FMA = true: the same kernel with the products on the CUDA cores (fp32 FMA,
+// warp-shuffle softmax) instead of mma.sync; kept to measure that choice.
+template <int D, bool FMA = false>
 struct DraftCfg {
     static constexpr int TK = kKeyTile;                 // keys per stage
     static constexpr int NW = kConsumerWarps;           // compute warps
@@ -83,11 +85,15 @@ struct DraftCfg {
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
     static constexpr int FLAG_OFF = BAR_OFF + 2 * STAGES * 8;
     static constexpr int RED_OFF = FLAG_OFF + 16;       // m[NW][8], l[NW][8]
-    static constexpr int TOTAL = RED_OFF + 2 * NW * kDraftRows * 4 + 1024;  // + slack to 1024-align
+    static constexpr int Q32_OFF = RED_OFF + 2 * NW * kDraftRows * 4;       // FMA: Q as fp32 [8][D]
+    static constexpr int PS_OFF = Q32_OFF + (FMA ? kDraftRows * D * 4 : 0);  // FMA: P [NW][16 keys][8 rows]
+    static constexpr int TOTAL = PS_OFF + (FMA ? NW * KW * kDraftRows * 4 : 0) + 1024;  // + slack to 1024-align
+    static constexpr int DL = D / 32;                   // FMA: head-dim columns per lane in P.V
     static_assert(KW == 16, "one m16 block of keys per warp");
     static_assert(OB_BYTES <= STAGES * STAGE_BYTES, "the combine reuses the staging area");
     static_assert(STAGES >= 2, "double buffering at least");
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
+    static_assert(Q32_OFF % 16 == 0 && PS_OFF % 16 == 0, "16-byte vectors");
 };
 
 __device__ __forceinline__ void draft_report(int32_t *err, int32_t code) {
@@ -99,12 +105,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int D, bool STEP>
-__global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
+template <int D, bool STEP, bool FMA>
+__global__ void __launch_bounds__(kThreads, DraftCfg<D, FMA>::MIN_BLOCKS)
     draft_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2,
                  const AttnParams p) {
-    using C = DraftCfg<D>;
+    using C = DraftCfg<D, FMA>;
     constexpr int TK = C::TK;
 
     extern __shared__ uint8_t smem_raw[];
@@ -236,7 +242,23 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     // Q^T as the B operand of every S^T product: k-step kk holds
     // Q[row g][kk*16 + 2*t4 + {0,1}] and Q[row g][kk*16 + 8 + 2*t4 + {0,1}]
     uint32_t qf[C::KSTEPS][2];
-    {
+    if constexpr (FMA) {
+        // Q as fp32 in shared memory [8 rows][D] (zero rows past the real ones),
+        // read by every lane of a row group at once
+        float *q32 = reinterpret_cast<float *>(gbase + C::Q32_OFF);
+        for (int i = threadIdx.x; i < kDraftRows * D / 8; i += NCT) {
+            const int r = i / (D / 8), v = i - r * (D / 8);
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.rows)
+                x = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                           ((int64_t)b * p.n_q_heads + kvh * p.group + r) * D) + v);
+            float4 *dst = reinterpret_cast<float4 *>(q32 + r * D + v * 8);
+            dst[0] = make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u),
+                                 __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+            dst[1] = make_float4(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xffff0000u),
+                                 __uint_as_float(x.w << 16), __uint_as_float(x.w & 0xffff0000u));
+        }
+    } else {
         const bool real = g < p.rows;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
             static_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)b * p.n_q_heads + kvh * p.group + (real ? g : 0)) * D);
@@ -277,160 +299,330 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     const int32_t new_rel = has_new ? (int32_t)(new_slot - k_begin) : -1;
     auto tag_ok = [&](int32_t t) { return t >= 0 && t <= qp && (t < sink || t > lo); };
 
-    // ldmatrix row addresses (this lane's row of its 8x8 matrix) within a
-    // stage, for k-steps / head-dim blocks 0..3 of each 64-column chunk; the
-    // chunk adds a constant TK * 128 bytes.  Rows are 16w + (0 or 8) + lr, so
-    // a row's 128-byte swizzle phase is lr.
-    uint32_t koff[4], voff[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int krow = C::KW * warp + (lm & 1) * 8 + lr;  // S^T: A = K[16 keys x 16 dims]
-        koff[c] = krow * 128 + ((((2 * c + (lm >> 1)) & 7) ^ lr) << 4);
-        const int vrow = C::KW * warp + (lm >> 1) * 8 + lr;  // O^T: A = V^T[16 dims x 16 keys] (transposed load)
-        voff[c] = vrow * 128 + ((((2 * c + (lm & 1)) & 7) ^ lr) << 4);
-    }
-
-    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows 2*t4 and 2*t4 + 1
-    float m_use[2] = {0.f, 0.f};                      // m_run, or 0 while it is -inf
-    float l_run[2] = {0.f, 0.f};                      // this thread's keys only
+    // running state: mma.sync path (rows 2*t4, 2*t4 + 1 of the S^T fragment)
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
+    float l_run[2] = {0.f, 0.f};  // this thread's keys only
     float oacc[C::KSTEPS][4];
-#pragma unroll
-    for (int i = 0; i < C::KSTEPS; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
+    // CUDA-core path: rows 4*rg .. 4*rg + 3 of this lane's key; O over 8 rows x DL columns
+    float fm_run[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+    float fl_run[4] = {0.f, 0.f, 0.f, 0.f};
+    float fo[kDraftRows][C::DL];
     const float kRaise = 8.f;  // log2 units: raise the running max only past 2^8
 
-    for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % C::STAGES;
-        int32_t nt0 = -1, nt1 = -1;
-        if (t + 1 < n_tiles) load_tags(t + 1, nt0, nt1);
-        bool live = !*abort_flag;
-        if (live && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
-            draft_report(p.err, WM_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            live = false;
+    if constexpr (!FMA) {
+        // ldmatrix row addresses (this lane's row of its 8x8 matrix) within a
+        // stage, for k-steps / head-dim blocks 0..3 of each 64-column chunk; the
+        // chunk adds a constant TK * 128 bytes.  Rows are 16w + (0 or 8) + lr, so
+        // a row's 128-byte swizzle phase is lr.
+        uint32_t koff[4], voff[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int krow = C::KW * warp + (lm & 1) * 8 + lr;  // S^T: A = K[16 keys x 16 dims]
+            koff[c] = krow * 128 + ((((2 * c + (lm >> 1)) & 7) ^ lr) << 4);
+            const int vrow = C::KW * warp + (lm >> 1) * 8 + lr;  // O^T: A = V^T[16 dims x 16 keys] (transposed load)
+            voff[c] = vrow * 128 + ((((2 * c + (lm & 1)) & 7) ^ lr) << 4);
         }
-        const int32_t kt = t * TK;  // the tile's first key, relative to the split
-        const uint32_t sK = sbase + s * C::STAGE_BYTES;
-        const uint32_t sV = sK + C::TILE_BYTES;
-        bool wrote_smem = false;
-        if (live) {
-            // ---- STEP: the appended rows replace the ring's stale row in the staged tile
-            if (STEP && new_rel >= kt + C::KW * warp && new_rel < kt + C::KW * warp + C::KW) {
-                const int row = new_rel - kt;
-#pragma unroll
-                for (int j = 0; j < VPL; ++j) {
-                    const int i = lane + 32 * j;
-                    if (i < NV) {
-                        const int v = i % (D / 8);
-                        st_shared_v4((i < D / 8 ? sK : sV) + (v >> 3) * (TK * 128) + swz128(row, v & 7), new_v[j]);
-                    }
-                }
-                __syncwarp();
-                wrote_smem = true;
-            }
 
-            // ---- S^T = K Q^T for this warp's 16 keys (two accumulator chains)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        float m_use[2] = {0.f, 0.f};                      // m_run, or 0 while it is -inf
 #pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(sK + koff[kk & 3] + (kk >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
-                mma_bf16((kk & 1) ? sb : sa, a, qf[kk][0], qf[kk][1]);
-            }
-            // masks of this thread's two keys: memory tiles hold only keys; ring
-            // keys are judged by their tags (the appended slot holds qpos)
-            const int32_t k0 = kt + kw_lane, k1 = k0 + 8;
-            bool ok0, ok1;
-            if (kt >= mem_rel) {
-                ok0 = k0 < klen;
-                ok1 = k1 < klen;
-            } else {
-                ok0 = k0 < klen && tag_ok(STEP && k0 == new_rel ? qp : tg0);
-                ok1 = k1 < klen && tag_ok(STEP && k1 == new_rel ? qp : tg1);
-            }
-            // sv[0], sv[1]: key g, rows 2t4 and 2t4+1; sv[2], sv[3]: key g + 8
-            float sv[4];
-            sv[0] = ok0 ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
-            sv[1] = ok0 ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
-            sv[2] = ok1 ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
-            sv[3] = ok1 ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
-            // ---- tile max per row over the warp's 16 keys
-            float tmax[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
+        for (int i = 0; i < C::KSTEPS; ++i)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 4));
-                tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 8));
-                tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 16));
+            for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
+
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % C::STAGES;
+            int32_t nt0 = -1, nt1 = -1;
+            if (t + 1 < n_tiles) load_tags(t + 1, nt0, nt1);
+            bool live = !*abort_flag;
+            if (live && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
+                draft_report(p.err, WM_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                live = false;
             }
-            // ---- raise the running max (rarely: only past 2^8), rescaling O^T and l
-            const bool raise0 = tmax[0] > m_run[0] + kRaise, raise1 = tmax[1] > m_run[1] + kRaise;
-            if (__any_sync(0xffffffffu, raise0 || raise1)) {
-                float alpha[2];
-                const bool rz[2] = {raise0, raise1};
+            const int32_t kt = t * TK;  // the tile's first key, relative to the split
+            const uint32_t sK = sbase + s * C::STAGE_BYTES;
+            const uint32_t sV = sK + C::TILE_BYTES;
+            bool wrote_smem = false;
+            if (live) {
+                // ---- STEP: the appended rows replace the ring's stale row in the staged tile
+                if (STEP && new_rel >= kt + C::KW * warp && new_rel < kt + C::KW * warp + C::KW) {
+                    const int row = new_rel - kt;
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) {
+                        const int i = lane + 32 * j;
+                        if (i < NV) {
+                            const int v = i % (D / 8);
+                            st_shared_v4((i < D / 8 ? sK : sV) + (v >> 3) * (TK * 128) + swz128(row, v & 7), new_v[j]);
+                        }
+                    }
+                    __syncwarp();
+                    wrote_smem = true;
+                }
+
+                // ---- S^T = K Q^T for this warp's 16 keys (two accumulator chains)
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(sK + koff[kk & 3] + (kk >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
+                    mma_bf16((kk & 1) ? sb : sa, a, qf[kk][0], qf[kk][1]);
+                }
+                // masks of this thread's two keys: memory tiles hold only keys; ring
+                // keys are judged by their tags (the appended slot holds qpos)
+                const int32_t k0 = kt + kw_lane, k1 = k0 + 8;
+                bool ok0, ok1;
+                if (kt >= mem_rel) {
+                    ok0 = k0 < klen;
+                    ok1 = k1 < klen;
+                } else {
+                    ok0 = k0 < klen && tag_ok(STEP && k0 == new_rel ? qp : tg0);
+                    ok1 = k1 < klen && tag_ok(STEP && k1 == new_rel ? qp : tg1);
+                }
+                // sv[0], sv[1]: key g, rows 2t4 and 2t4+1; sv[2], sv[3]: key g + 8
+                float sv[4];
+                sv[0] = ok0 ? (sa[0] + sb[0]) * p.scale_log2 : -CUDART_INF_F;
+                sv[1] = ok0 ? (sa[1] + sb[1]) * p.scale_log2 : -CUDART_INF_F;
+                sv[2] = ok1 ? (sa[2] + sb[2]) * p.scale_log2 : -CUDART_INF_F;
+                sv[3] = ok1 ? (sa[3] + sb[3]) * p.scale_log2 : -CUDART_INF_F;
+                // ---- tile max per row over the warp's 16 keys
+                float tmax[2] = {fmaxf(sv[0], sv[2]), fmaxf(sv[1], sv[3])};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float mn = rz[h] ? tmax[h] : m_run[h];
-                    alpha[h] = rz[h] ? ex2(m_run[h] - mn) : 1.f;  // 0 when m_run was -inf
-                    m_run[h] = mn;
-                    m_use[h] = mn == -CUDART_INF_F ? 0.f : mn;
-                    l_run[h] *= alpha[h];
+                    tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 4));
+                    tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 8));
+                    tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 16));
                 }
+                // ---- raise the running max (rarely: only past 2^8), rescaling O^T and l
+                const bool raise0 = tmax[0] > m_run[0] + kRaise, raise1 = tmax[1] > m_run[1] + kRaise;
+                if (__any_sync(0xffffffffu, raise0 || raise1)) {
+                    float alpha[2];
+                    const bool rz[2] = {raise0, raise1};
 #pragma unroll
-                for (int i = 0; i < C::KSTEPS; ++i) {
-                    oacc[i][0] *= alpha[0];
-                    oacc[i][1] *= alpha[1];
-                    oacc[i][2] *= alpha[0];
-                    oacc[i][3] *= alpha[1];
+                    for (int h = 0; h < 2; ++h) {
+                        const float mn = rz[h] ? tmax[h] : m_run[h];
+                        alpha[h] = rz[h] ? ex2(m_run[h] - mn) : 1.f;  // 0 when m_run was -inf
+                        m_run[h] = mn;
+                        m_use[h] = mn == -CUDART_INF_F ? 0.f : mn;
+                        l_run[h] *= alpha[h];
+                    }
+#pragma unroll
+                    for (int i = 0; i < C::KSTEPS; ++i) {
+                        oacc[i][0] *= alpha[0];
+                        oacc[i][1] *= alpha[1];
+                        oacc[i][2] *= alpha[0];
+                        oacc[i][3] *= alpha[1];
+                    }
+                }
+                const float p0 = ex2(sv[0] - m_use[0]), p1 = ex2(sv[1] - m_use[1]);
+                const float p2 = ex2(sv[2] - m_use[0]), p3 = ex2(sv[3] - m_use[1]);
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
+                // ---- P^T as the B operand: hi and lo bf16 parts, transposed in registers
+                const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+                const __nv_bfloat162 hb01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
+                const __nv_bfloat162 hb23 = *reinterpret_cast<const __nv_bfloat162 *>(&h23);
+                const uint32_t l01 = pack_bf16(p0 - __low2float(hb01), p1 - __high2float(hb01));
+                const uint32_t l23 = pack_bf16(p2 - __low2float(hb23), p3 - __high2float(hb23));
+                const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
+                const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
+                // ---- keys masked for every row: their V^T operand elements are
+                // zeroed (only on tiles that have such keys)
+                const uint32_t okb0 = __ballot_sync(0xffffffffu, ok0), okb1 = __ballot_sync(0xffffffffu, ok1);
+                if ((okb0 & okb1) == 0xffffffffu) {
+#pragma unroll
+                    for (int i = 0; i < C::KSTEPS; ++i) {
+                        uint32_t a[4];
+                        ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
+                        mma_bf16(oacc[i], a, bh0, bh1);
+                        mma_bf16(oacc[i], a, bl0, bl1);
+                    }
+                } else {
+                    // this thread's V^T columns: keys 2t4, 2t4+1 (a0, a1) and 2t4+8, 2t4+9 (a2, a3)
+                    const uint32_t mlo = (((okb0 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                         (((okb0 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
+                    const uint32_t mhi = (((okb1 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
+                                         (((okb1 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int i = 0; i < C::KSTEPS; ++i) {
+                        uint32_t a[4];
+                        ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
+                        a[0] &= mlo;
+                        a[1] &= mlo;
+                        a[2] &= mhi;
+                        a[3] &= mhi;
+                        mma_bf16(oacc[i], a, bh0, bh1);
+                        mma_bf16(oacc[i], a, bl0, bl1);
+                    }
                 }
             }
-            const float p0 = ex2(sv[0] - m_use[0]), p1 = ex2(sv[1] - m_use[1]);
-            const float p2 = ex2(sv[2] - m_use[0]), p3 = ex2(sv[3] - m_use[1]);
-            l_run[0] += p0 + p2;
-            l_run[1] += p1 + p3;
-            // ---- P^T as the B operand: hi and lo bf16 parts, transposed in registers
-            const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-            const __nv_bfloat162 hb01 = *reinterpret_cast<const __nv_bfloat162 *>(&h01);
-            const __nv_bfloat162 hb23 = *reinterpret_cast<const __nv_bfloat162 *>(&h23);
-            const uint32_t l01 = pack_bf16(p0 - __low2float(hb01), p1 - __high2float(hb01));
-            const uint32_t l23 = pack_bf16(p2 - __low2float(hb23), p3 - __high2float(hb23));
-            const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
-            const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
-            // ---- keys masked for every row: their V^T operand elements are
-            // zeroed (only on tiles that have such keys)
-            const uint32_t okb0 = __ballot_sync(0xffffffffu, ok0), okb1 = __ballot_sync(0xffffffffu, ok1);
-            if ((okb0 & okb1) == 0xffffffffu) {
-#pragma unroll
-                for (int i = 0; i < C::KSTEPS; ++i) {
-                    uint32_t a[4];
-                    ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
-                    mma_bf16(oacc[i], a, bh0, bh1);
-                    mma_bf16(oacc[i], a, bl0, bl1);
-                }
-            } else {
-                // this thread's V^T columns: keys 2t4, 2t4+1 (a0, a1) and 2t4+8, 2t4+9 (a2, a3)
-                const uint32_t mlo = (((okb0 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
-                                     (((okb0 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
-                const uint32_t mhi = (((okb1 >> (8 * t4)) & 1u) ? 0x0000ffffu : 0u) |
-                                     (((okb1 >> (8 * t4 + 4)) & 1u) ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int i = 0; i < C::KSTEPS; ++i) {
-                    uint32_t a[4];
-                    ldsm_x4_t(sV + voff[i & 3] + (i >> 2) * (TK * 128), a[0], a[1], a[2], a[3]);
-                    a[0] &= mlo;
-                    a[1] &= mlo;
-                    a[2] &= mhi;
-                    a[3] &= mhi;
-                    mma_bf16(oacc[i], a, bh0, bh1);
-                    mma_bf16(oacc[i], a, bl0, bl1);
-                }
-            }
+            if (wrote_smem) fence_proxy_async_smem();  // the stage is refilled by TMA later
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            tg0 = nt0;
+            tg1 = nt1;
         }
-        if (wrote_smem) fence_proxy_async_smem();  // the stage is refilled by TMA later
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        tg0 = nt0;
-        tg1 = nt1;
+    } else {
+        // ================= CUDA-core products (fp32 FMA, warp-shuffle softmax)
+        // Lane (kl, rg) = (lane & 15, lane >> 4) computes S for key 16w + kl and
+        // rows 4rg .. 4rg + 3; for P.V the lane owns DL head-dim columns of all
+        // 8 rows and reads P back from a per-warp shared buffer.
+        const int kl = lane & 15, rg = lane >> 4;
+        const int krow = C::KW * warp + kl;  // this lane's key row in a tile
+        const float4 *q32 = reinterpret_cast<const float4 *>(gbase + C::Q32_OFF);
+        float *ps = reinterpret_cast<float *>(gbase + C::PS_OFF) + warp * C::KW * kDraftRows;
+        const int32_t *ftags = tags;
+        auto load_tag = [&](int t) -> int32_t {
+            const int32_t ka = t * TK + krow;
+            return ka < ring_rel ? __ldg(ftags + ka) : -1;
+        };
+        int32_t ftg = n_tiles > 0 ? load_tag(0) : -1;
+        float fm_use[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < kDraftRows; ++r)
+#pragma unroll
+            for (int j = 0; j < C::DL; ++j) fo[r][j] = 0.f;
+        named_bar_sync(1, NCT);  // Q staged
+        const int dcol = lane * C::DL;  // first head-dim column of this lane in P.V
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % C::STAGES;
+            const int32_t nftg = t + 1 < n_tiles ? load_tag(t + 1) : -1;
+            bool live = !*abort_flag;
+            if (live && !mbar_wait_bounded(bar_full + 8 * s, (t / C::STAGES) & 1, p.wait_limit)) {
+                draft_report(p.err, WM_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                live = false;
+            }
+            const int32_t kt = t * TK;
+            const uint32_t sK = sbase + s * C::STAGE_BYTES;
+            const uint32_t sV = sK + C::TILE_BYTES;
+            const uint8_t *tK = gbase + (sK - sbase);
+            const uint8_t *tV = tK + C::TILE_BYTES;
+            bool wrote_smem = false;
+            if (live) {
+                if (STEP && new_rel >= kt + C::KW * warp && new_rel < kt + C::KW * warp + C::KW) {
+                    const int row = new_rel - kt;
+#pragma unroll
+                    for (int j = 0; j < VPL; ++j) {
+                        const int i = lane + 32 * j;
+                        if (i < NV) {
+                            const int v = i % (D / 8);
+                            st_shared_v4((i < D / 8 ? sK : sV) + (v >> 3) * (TK * 128) + swz128(row, v & 7),
+                                         new_v[j]);
+                        }
+                    }
+                    __syncwarp();
+                    wrote_smem = true;
+                }
+                // ---- S for this lane's key and four rows: dot products over D
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 kv = *reinterpret_cast<const uint4 *>(tK + (c >> 3) * (TK * 128) + swz128(krow, c & 7));
+                    const float k0 = __uint_as_float(kv.x << 16), k1 = __uint_as_float(kv.x & 0xffff0000u);
+                    const float k2 = __uint_as_float(kv.y << 16), k3 = __uint_as_float(kv.y & 0xffff0000u);
+                    const float k4 = __uint_as_float(kv.z << 16), k5 = __uint_as_float(kv.z & 0xffff0000u);
+                    const float k6 = __uint_as_float(kv.w << 16), k7 = __uint_as_float(kv.w & 0xffff0000u);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 qa = q32[(4 * rg + i) * (D / 4) + 2 * c];
+                        const float4 qb = q32[(4 * rg + i) * (D / 4) + 2 * c + 1];
+                        float a = acc[i];
+                        a = fmaf(qa.x, k0, a);
+                        a = fmaf(qa.y, k1, a);
+                        a = fmaf(qa.z, k2, a);
+                        a = fmaf(qa.w, k3, a);
+                        a = fmaf(qb.x, k4, a);
+                        a = fmaf(qb.y, k5, a);
+                        a = fmaf(qb.z, k6, a);
+                        a = fmaf(qb.w, k7, a);
+                        acc[i] = a;
+                    }
+                }
+                const int32_t kk = kt + krow;
+                const bool ok = kt >= mem_rel ? kk < klen : (kk < klen && tag_ok(STEP && kk == new_rel ? qp : ftg));
+                float sv[4], tmax[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sv[i] = ok ? acc[i] * p.scale_log2 : -CUDART_INF_F;
+                    float m = sv[i];  // max over the warp's 16 keys (the 16 lanes of this row group)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    tmax[i] = m;
+                }
+                bool rz[4], any_rz = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    rz[i] = tmax[i] > fm_run[i] + kRaise;
+                    any_rz |= rz[i];
+                }
+                if (__any_sync(0xffffffffu, any_rz)) {
+                    float al[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float mn = rz[i] ? tmax[i] : fm_run[i];
+                        al[i] = rz[i] ? ex2(fm_run[i] - mn) : 1.f;
+                        fm_run[i] = mn;
+                        fm_use[i] = mn == -CUDART_INF_F ? 0.f : mn;
+                        fl_run[i] *= al[i];
+                    }
+                    // P.V rows: this group's four and, by exchange, the other group's
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float other = __shfl_xor_sync(0xffffffffu, al[i], 16);
+                        const float a_lo = rg ? other : al[i], a_hi = rg ? al[i] : other;
+#pragma unroll
+                        for (int j = 0; j < C::DL; ++j) {
+                            fo[i][j] *= a_lo;
+                            fo[4 + i][j] *= a_hi;
+                        }
+                    }
+                }
+                float pr[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pr[i] = ex2(sv[i] - fm_use[i]);
+                    fl_run[i] += pr[i];
+                }
+                *reinterpret_cast<float4 *>(ps + kl * kDraftRows + 4 * rg) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+                const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;  // keys of the warp with weight
+                __syncwarp();
+                // ---- O += P V over this lane's DL columns of the 8 rows
+#pragma unroll 2
+                for (int k = 0; k < C::KW; ++k) {
+                    if (!((vm >> k) & 1u)) continue;  // masked for every row: its V bytes are never read
+                    const int vrow = C::KW * warp + k;
+                    const uint8_t *vp = tV + (dcol >> 6) * (TK * 128) + swz128(vrow, (dcol & 63) >> 3) + (dcol & 7) * 2;
+                    float vf[C::DL];
+                    if constexpr (C::DL == 8) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(vp);
+                        vf[0] = __uint_as_float(x.x << 16); vf[1] = __uint_as_float(x.x & 0xffff0000u);
+                        vf[2] = __uint_as_float(x.y << 16); vf[3] = __uint_as_float(x.y & 0xffff0000u);
+                        vf[4] = __uint_as_float(x.z << 16); vf[5] = __uint_as_float(x.z & 0xffff0000u);
+                        vf[6] = __uint_as_float(x.w << 16); vf[7] = __uint_as_float(x.w & 0xffff0000u);
+                    } else if constexpr (C::DL == 4) {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(vp);
+                        vf[0] = __uint_as_float(x.x << 16); vf[1] = __uint_as_float(x.x & 0xffff0000u);
+                        vf[2] = __uint_as_float(x.y << 16); vf[3] = __uint_as_float(x.y & 0xffff0000u);
+                    } else {
+                        const uint32_t x = *reinterpret_cast<const uint32_t *>(vp);
+                        vf[0] = __uint_as_float(x << 16); vf[1] = __uint_as_float(x & 0xffff0000u);
+                    }
+                    const float4 pa = *reinterpret_cast<const float4 *>(ps + k * kDraftRows);
+                    const float4 pb = *reinterpret_cast<const float4 *>(ps + k * kDraftRows + 4);
+                    const float pk[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+                    for (int r = 0; r < kDraftRows; ++r)
+#pragma unroll
+                        for (int j = 0; j < C::DL; ++j) fo[r][j] = fmaf(pk[r], vf[j], fo[r][j]);
+                }
+            }
+            if (wrote_smem) fence_proxy_async_smem();  // the stage is refilled by TMA later
+            __syncwarp();  // every lane has read this tile's P before the next tile writes it
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            ftg = nftg;
+        }
     }
 
     // ---- STEP: store the appended entry into the ring (the owning warp; every
@@ -451,18 +643,36 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
         }
     }
 
-    // ---- combine the four warps: row maxima and sums, then O^T in a fixed order
+    // ---- combine the four warps: row maxima and sums, then O in a fixed order
+    if constexpr (!FMA) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
-    }
-    if (g == 0) {
-        red_m[warp * kDraftRows + 2 * t4] = m_run[0];
-        red_m[warp * kDraftRows + 2 * t4 + 1] = m_run[1];
-        red_l[warp * kDraftRows + 2 * t4] = l_run[0];
-        red_l[warp * kDraftRows + 2 * t4 + 1] = l_run[1];
+        for (int h = 0; h < 2; ++h) {
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+        }
+        if (g == 0) {
+            red_m[warp * kDraftRows + 2 * t4] = m_run[0];
+            red_m[warp * kDraftRows + 2 * t4 + 1] = m_run[1];
+            red_l[warp * kDraftRows + 2 * t4] = l_run[0];
+            red_l[warp * kDraftRows + 2 * t4 + 1] = l_run[1];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            fl_run[i] += __shfl_xor_sync(0xffffffffu, fl_run[i], 1);
+            fl_run[i] += __shfl_xor_sync(0xffffffffu, fl_run[i], 2);
+            fl_run[i] += __shfl_xor_sync(0xffffffffu, fl_run[i], 4);
+            fl_run[i] += __shfl_xor_sync(0xffffffffu, fl_run[i], 8);
+        }
+        if ((lane & 15) == 0) {
+            const int r0 = 4 * (lane >> 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                red_m[warp * kDraftRows + r0 + i] = fm_run[i];
+                red_l[warp * kDraftRows + r0 + i] = fl_run[i];
+            }
+        }
     }
     // After an aborted pipeline, copies may still land in the staging area:
     // this CTA's result is then not written (the decision is the same in
@@ -470,23 +680,36 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     const bool aborted = named_bar_sync_or(1, NCT, *abort_flag != 0);
     float *obuf = reinterpret_cast<float *>(gbase);  // the staging area: every copy has landed and been read
     if (!aborted) {
-        float f[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = 2 * t4 + h;
-            float mx = red_m[r];
-#pragma unroll
-            for (int w = 1; w < C::NW; ++w) mx = fmaxf(mx, red_m[w * kDraftRows + r]);
-            f[h] = m_run[h] == -CUDART_INF_F ? 0.f : ex2(m_run[h] - mx);
-        }
         float *ob = obuf + warp * kDraftRows * C::OB_STRIDE;
+        if constexpr (!FMA) {
+            float f[2];
 #pragma unroll
-        for (int i = 0; i < C::KSTEPS; ++i) {
-            const int d = i * 16 + g;
-            ob[(2 * t4) * C::OB_STRIDE + d] = oacc[i][0] * f[0];
-            ob[(2 * t4 + 1) * C::OB_STRIDE + d] = oacc[i][1] * f[1];
-            ob[(2 * t4) * C::OB_STRIDE + d + 8] = oacc[i][2] * f[0];
-            ob[(2 * t4 + 1) * C::OB_STRIDE + d + 8] = oacc[i][3] * f[1];
+            for (int h = 0; h < 2; ++h) {
+                const int r = 2 * t4 + h;
+                float mx = red_m[r];
+#pragma unroll
+                for (int w = 1; w < C::NW; ++w) mx = fmaxf(mx, red_m[w * kDraftRows + r]);
+                f[h] = m_run[h] == -CUDART_INF_F ? 0.f : ex2(m_run[h] - mx);
+            }
+#pragma unroll
+            for (int i = 0; i < C::KSTEPS; ++i) {
+                const int d = i * 16 + g;
+                ob[(2 * t4) * C::OB_STRIDE + d] = oacc[i][0] * f[0];
+                ob[(2 * t4 + 1) * C::OB_STRIDE + d] = oacc[i][1] * f[1];
+                ob[(2 * t4) * C::OB_STRIDE + d + 8] = oacc[i][2] * f[0];
+                ob[(2 * t4 + 1) * C::OB_STRIDE + d + 8] = oacc[i][3] * f[1];
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < kDraftRows; ++r) {
+                const float mw = red_m[warp * kDraftRows + r];
+                float mx = red_m[r];
+#pragma unroll
+                for (int w = 1; w < C::NW; ++w) mx = fmaxf(mx, red_m[w * kDraftRows + r]);
+                const float f = mw == -CUDART_INF_F ? 0.f : ex2(mw - mx);
+#pragma unroll
+                for (int j = 0; j < C::DL; ++j) ob[r * C::OB_STRIDE + lane * C::DL + j] = fo[r][j] * f;
+            }
         }
     }
     named_bar_sync(1, NCT);
@@ -545,34 +768,34 @@ __global__ void __launch_bounds__(kThreads, DraftCfg<D>::MIN_BLOCKS)
     }
 }
 
-template <int D, bool STEP>
+template <int D, bool STEP, bool FMA>
 cudaError_t launch_draft_kernel(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const AttnParams &p, cudaStream_t stream) {
-    constexpr int smem = DraftCfg<D>::TOTAL;
+    constexpr int smem = DraftCfg<D, FMA>::TOTAL;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(draft_kernel<D, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(draft_kernel<D, STEP, FMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const dim3 grid(p.n_split, p.batch * p.n_kv_heads);
-    return launch_pdl(draft_kernel<D, STEP>, grid, dim3(kThreads), smem, stream, k, v, mk, mv, p);
+    return launch_pdl(draft_kernel<D, STEP, FMA>, grid, dim3(kThreads), smem, stream, k, v, mk, mv, p);
 }
 
-template <int D, bool STEP>
+template <int D, bool STEP, bool FMA>
 int draft_blocks_per_sm_t() {
-    constexpr int smem = DraftCfg<D>::TOTAL;
-    if (cudaFuncSetAttribute(draft_kernel<D, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    constexpr int smem = DraftCfg<D, FMA>::TOTAL;
+    if (cudaFuncSetAttribute(draft_kernel<D, STEP, FMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<D, STEP>, kThreads, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<D, STEP, FMA>, kThreads, smem) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

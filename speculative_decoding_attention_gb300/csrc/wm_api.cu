@@ -21,6 +21,9 @@ __device__ int32_t g_device_error;  // first device-side data error (WM_DEVERR_*
 // the timeout path.
 thread_local uint32_t t_wait_limit = kWaitLimit;
 thread_local int32_t t_stall_tile = -1;
+// Arithmetic of the keys-as-M draft kernel for this host thread's calls
+// (wm_set_draft_math): tensor cores (default) or CUDA cores.
+thread_local int32_t t_draft_math = WM_DRAFT_MATH_MMA;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRows = 64;  // query rows per KV head (4 m-tiles of 16)
@@ -151,7 +154,7 @@ constexpr int64_t kRaggedSplitBytes = 8ll << 20;
 int ctas_per_sm(int op, int head_dim, int rows) {
     static std::mutex mu;
     static int cache[kMaxDevices][3][4][2] = {};
-    static int draft_cache[kMaxDevices][3] = {};
+    static int draft_cache[kMaxDevices][3][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
@@ -159,11 +162,12 @@ int ctas_per_sm(int op, int head_dim, int rows) {
     const int oi = op == WM_OP_VERIFY ? 1 : 0;
     std::lock_guard<std::mutex> lock(mu);
     if (use_draft_kernel(op, rows)) {
-        int &nd = draft_cache[dev][di];
+        const bool fma = t_draft_math == WM_DRAFT_MATH_FMA;
+        int &nd = draft_cache[dev][di][fma ? 1 : 0];
         if (!nd) {
             auto query = [&](bool step) {
-                return di == 0 ? draft_blocks_per_sm_d64(step)
-                     : di == 1 ? draft_blocks_per_sm_d128(step) : draft_blocks_per_sm_d256(step);
+                return di == 0 ? draft_blocks_per_sm_d64(step, fma)
+                     : di == 1 ? draft_blocks_per_sm_d128(step, fma) : draft_blocks_per_sm_d256(step, fma);
             };
             nd = std::max(1, std::min(query(false), query(true)));
         }
@@ -242,10 +246,11 @@ cudaError_t launch_attn_any(int op, const CUtensorMap (&maps)[4], const AttnPara
                             cudaStream_t st) {
     const int m_tiles = (p.rows + 15) / 16;
     if (use_draft_kernel(op, p.rows)) {
+        const bool fma = t_draft_math == WM_DRAFT_MATH_FMA;
         switch (p.head_dim) {
-            case 64: return launch_draft_d64(maps[0], maps[1], maps[2], maps[3], p, step, st);
-            case 128: return launch_draft_d128(maps[0], maps[1], maps[2], maps[3], p, step, st);
-            case 256: return launch_draft_d256(maps[0], maps[1], maps[2], maps[3], p, step, st);
+            case 64: return launch_draft_d64(maps[0], maps[1], maps[2], maps[3], p, step, fma, st);
+            case 128: return launch_draft_d128(maps[0], maps[1], maps[2], maps[3], p, step, fma, st);
+            case 256: return launch_draft_d256(maps[0], maps[1], maps[2], maps[3], p, step, fma, st);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -328,6 +333,12 @@ const char *wm_status_string(wm_status s) {
 }
 
 int32_t wm_version(void) { return 100; }
+
+wm_status wm_set_draft_math(int32_t math) {
+    if (math != WM_DRAFT_MATH_MMA && math != WM_DRAFT_MATH_FMA) return WM_ERR_INVALID_ARG;
+    t_draft_math = math;
+    return WM_OK;
+}
 
 wm_status wm_set_test_stall(int32_t stall_tile, uint32_t wait_polls) {
     if (stall_tile < -1 || (stall_tile >= 0 && wait_polls == 0)) return WM_ERR_INVALID_ARG;

@@ -96,18 +96,19 @@ cudaError_t launch_attn_d256(const CUtensorMap &k, const CUtensorMap &v, const C
 
 // Keys-as-M draft kernel (draft_d<D>.cu) for up to kDraftRowsMax query rows per
 // KV head: the plain draft attention, or (step) the fused draft step, which
-// always writes split partials.
+// always writes split partials; fma selects the CUDA-core variant of its
+// products (measurement only) instead of mma.sync.
 constexpr int kDraftRowsMax = 8;
 cudaError_t launch_draft_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
-                             const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+                             const CUtensorMap &mv, const AttnParams &p, bool step, bool fma, cudaStream_t stream);
 cudaError_t launch_draft_d128(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
-                              const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+                              const CUtensorMap &mv, const AttnParams &p, bool step, bool fma, cudaStream_t stream);
 cudaError_t launch_draft_d256(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &mk,
-                              const CUtensorMap &mv, const AttnParams &p, bool step, cudaStream_t stream);
+                              const CUtensorMap &mv, const AttnParams &p, bool step, bool fma, cudaStream_t stream);
 // Resident CTAs per SM of that kernel (0 if unknown).
-int draft_blocks_per_sm_d64(bool step);
-int draft_blocks_per_sm_d128(bool step);
-int draft_blocks_per_sm_d256(bool step);
+int draft_blocks_per_sm_d64(bool step, bool fma);
+int draft_blocks_per_sm_d128(bool step, bool fma);
+int draft_blocks_per_sm_d256(bool step, bool fma);
 
 // Resident CTAs per SM of the mma.sync attention kernel for head dim D with
 // m_tiles row tiles (step: the fused draft-step instance); 0 if unknown.

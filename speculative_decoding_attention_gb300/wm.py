@@ -18,12 +18,13 @@ from . import build as _build
 
 WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, WM_ERR_DEVICE_DATA = range(6)
 WM_OP_DRAFT, WM_OP_VERIFY, WM_OP_DRAFT_STEP, WM_OP_DRAFT_MEM = 0, 1, 2, 3
+WM_DRAFT_MATH_MMA, WM_DRAFT_MATH_FMA = 0, 1
 DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout", 4: "internal check"}
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
             "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
             "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step", "wm_draft_attn_mem",
-            "wm_mem_append", "wm_mem_rollback", "wm_set_test_stall")
+            "wm_mem_append", "wm_mem_rollback", "wm_set_test_stall", "wm_set_draft_math")
 STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
 
 _lib = None
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
         lib.wm_version.restype = I32
         lib.wm_set_test_stall.argtypes = [I32, ctypes.c_uint32]
         lib.wm_set_test_stall.restype = I32
+        lib.wm_set_draft_math.argtypes = [I32]
+        lib.wm_set_draft_math.restype = I32
         for name in ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_draft_attn_static",
                      "wm_verify_attn", "wm_lse_merge", "wm_get_device_error"):
             getattr(lib, name).restype = I32
@@ -445,6 +448,13 @@ def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out=None, lse=None
                                n_parts, rows, D, _dev(out, torch.bfloat16, "out"),
                                _dev(lse, torch.float32, "lse"), _stream(stream)), "wm_lse_merge")
     return out, lse
+
+
+def set_draft_math(math: int) -> None:
+    """The draft kernel's arithmetic for this thread's draft calls:
+    WM_DRAFT_MATH_MMA (tensor cores, the default) or WM_DRAFT_MATH_FMA (CUDA
+    cores; kept to measure the choice).  See wm_set_draft_math in include/wm_api.h."""
+    _check(load().wm_set_draft_math(int(math)), "wm_set_draft_math")
 
 
 def set_test_stall(stall_tile: int, wait_polls: int = 0) -> None:

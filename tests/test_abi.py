@@ -289,3 +289,10 @@ def test_test_stall_hook_rejects_bad_settings(lib):
     assert lib.wm_set_test_stall(0, 0) == wm.WM_ERR_INVALID_ARG
     assert lib.wm_set_test_stall(3, 100) == wm.WM_OK
     assert lib.wm_set_test_stall(-1, 0) == wm.WM_OK
+
+
+def test_draft_math_setting(lib):
+    assert lib.wm_set_draft_math(2) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_set_draft_math(-1) == wm.WM_ERR_INVALID_ARG
+    assert lib.wm_set_draft_math(wm.WM_DRAFT_MATH_FMA) == wm.WM_OK
+    assert lib.wm_set_draft_math(wm.WM_DRAFT_MATH_MMA) == wm.WM_OK
