@@ -204,47 +204,11 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
     const int kvh = unit - b * p.n_kv_heads;
     const int split = blockIdx.x;
 
-    pdl_wait();  // every global access below may depend on the previous kernel
-    pdl_launch_dependents();
-
-    int64_t n_keys, qpos0;
-    if (p.source == KEYS_RING) {
-        int64_t seen = p.n_seen[b];
-        if (seen < 0) {
-            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
-            seen = 0;
-        }
-        n_keys = p.n_slots;
-        qpos0 = seen - 1;
-    } else {
-        int64_t len = p.seq_lens[b];
-        if (len < 0 || len > p.capacity) {
-            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
-            len = len < 0 ? 0 : p.capacity;
-        }
-        n_keys = len;
-        qpos0 = len - p.n_q;
-    }
-    const int64_t k_begin = (int64_t)split * p.keys_per_split;
-    const int64_t k_end = min(k_begin + (int64_t)p.keys_per_split, n_keys);
-    const int n_tiles = k_end > k_begin ? (int)((k_end - k_begin + TK - 1) / TK) : 0;
-
-    if (n_tiles == 0) {
-        // An empty split (past the end of a shorter sequence): record "no keys"
-        // for its rows and leave without touching tensor memory.
-        for (int r = threadIdx.x; r < p.rows; r += kTcThreads) {
-            const int qi = r / p.group, hh = r - qi * p.group;
-            const int64_t orow = ((int64_t)b * p.n_q + qi) * p.n_q_heads + kvh * p.group + hh;
-            if (p.o_part) {
-                p.lse_part[orow * p.n_split + split] = -CUDART_INF_F;
-            } else {
-                if (p.lse) p.lse[orow] = -CUDART_INF_F;
-                for (int d = 0; d < D; ++d) static_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(0.f);
-            }
-        }
-        return;
-    }
-
+    // Set-up that touches only shared and tensor memory runs before the wait
+    // on the previous kernel, while it drains: the pipeline barriers and this
+    // CTA's tensor-memory columns (an allocation that finds them still held by
+    // a draining CTA of the previous kernel waits for them; that kernel never
+    // waits on this one).
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NSLOT; ++s) {
             mbar_init(bar_full0 + 8 * s, 1);
@@ -273,6 +237,48 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tptr;
+
+    pdl_wait();  // every global access below may depend on the previous kernel
+    pdl_launch_dependents();
+    int64_t n_keys, qpos0;
+    if (p.source == KEYS_RING) {
+        int64_t seen = p.n_seen[b];
+        if (seen < 0) {
+            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
+            seen = 0;
+        }
+        n_keys = p.n_slots;
+        qpos0 = seen - 1;
+    } else {
+        int64_t len = p.seq_lens[b];
+        if (len < 0 || len > p.capacity) {
+            if (threadIdx.x == 0) tc_report(p.err, WM_DEVERR_BAD_LENGTH);
+            len = len < 0 ? 0 : p.capacity;
+        }
+        n_keys = len;
+        qpos0 = len - p.n_q;
+    }
+    const int64_t k_begin = (int64_t)split * p.keys_per_split;
+    const int64_t k_end = min(k_begin + (int64_t)p.keys_per_split, n_keys);
+    const int n_tiles = k_end > k_begin ? (int)((k_end - k_begin + TK - 1) / TK) : 0;
+
+    if (n_tiles == 0) {
+        // An empty split (past the end of a shorter sequence): record "no keys"
+        // for its rows, hand the tensor memory back and leave.
+        for (int r = threadIdx.x; r < p.rows; r += kTcThreads) {
+            const int qi = r / p.group, hh = r - qi * p.group;
+            const int64_t orow = ((int64_t)b * p.n_q + qi) * p.n_q_heads + kvh * p.group + hh;
+            if (p.o_part) {
+                p.lse_part[orow * p.n_split + split] = -CUDART_INF_F;
+            } else {
+                if (p.lse) p.lse[orow] = -CUDART_INF_F;
+                for (int d = 0; d < D; ++d) static_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(0.f);
+            }
+        }
+        if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+        return;
+    }
+
 
     if (warp == 0 || (C::SV && warp == 2 + NSW)) {
         // ======================================================== TMA producer
