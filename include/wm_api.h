@@ -382,12 +382,13 @@ wm_status wm_set_draft_math(int32_t math);
  * of polls the kernel records WM_DEVERR_TIMEOUT in the device error word,
  * stops its remaining work, waits (again bounded) for its own copies in
  * flight and returns, so a lost arrival can never hang the GPU.  This call
- * makes that path reachable on purpose: after it, the attention launches made
- * by the calling host thread through the mma.sync kernels (every draft call;
- * verification at head_dim 64) have their producer stop issuing copies at key
- * tile `stall_tile` of each split (a tile that then never arrives) and give up
- * a wait after `wait_polls` polls (about 0.1 us each, or more: a poll may
- * suspend the thread briefly).  stall_tile = -1 restores the defaults
+ * makes that path reachable on purpose: after it, every attention launch made
+ * by the calling host thread has its producer stop issuing copies at copy
+ * unit `stall_tile` of each split (a key tile in the mma.sync kernels; in the
+ * tcgen05 verify kernel a K or V tile, or a 64-key V half where V is staged
+ * in halves), so that unit never arrives, and gives up a wait after
+ * `wait_polls` polls (about 0.1 us each, or more: a poll may suspend the
+ * thread briefly).  stall_tile = -1 restores the defaults
  * (no stall, the production limit of 2^22 polls).  Outputs of a stalled call
  * are undefined; the context stays usable and the next call is normal.
  * Returns WM_ERR_INVALID_ARG for stall_tile < -1 or wait_polls = 0 with a stall.

@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             int64_t next_local = 0;
             int next_row = (int)(k_begin - first_page * p.page_size);
             for (int u = 0; u < n_units; ++u) {
+                if (u == p.stall_tile) break;  // tests of the timeout path only
                 const int s = u % nslot;
                 if (u >= nslot && !mbar_wait_bounded(empty0 + 8 * s, ((u / nslot) & 1) ^ 1, p.wait_limit)) {
                     tc_report(p.err, WM_DEVERR_TIMEOUT);
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 
             int next_row = (int)(k_begin - first_page * p.page_size);  // its first row in that page
             int box_page[2] = {0, 0}, box_row[2] = {0, 0};            // tile t's boxes (TK / box_rows <= 2)
             for (int u = 0; u < 2 * n_tiles; ++u) {
+                if (u == p.stall_tile) break;  // tests of the timeout path only
                 const int s = u % C::NSLOT;
                 if (u >= C::NSLOT &&
                     !mbar_wait_bounded(bar_empty0 + 8 * s, ((u / C::NSLOT) & 1) ^ 1, p.wait_limit)) {

@@ -458,10 +458,10 @@ def set_draft_math(math: int) -> None:
 
 
 def set_test_stall(stall_tile: int, wait_polls: int = 0) -> None:
-    """Tests of the timeout path only: make this thread's mma.sync attention
-    launches stop issuing copies at key tile ``stall_tile`` of each split and
-    give up a wait after ``wait_polls`` polls (``stall_tile=-1`` restores the
-    defaults).  See wm_set_test_stall in include/wm_api.h."""
+    """Tests of the timeout path only: make this thread's attention launches
+    stop issuing copies at copy unit ``stall_tile`` of each split and give up a
+    wait after ``wait_polls`` polls (``stall_tile=-1`` restores the defaults).
+    See wm_set_test_stall in include/wm_api.h."""
     _check(load().wm_set_test_stall(int(stall_tile), int(wait_polls)), "wm_set_test_stall")
 
 

@@ -1,6 +1,6 @@
 """The bounded-wait timeout path of the attention kernels, made reachable on
 purpose: a test hook (wm_set_test_stall) makes the producer warp stop issuing
-copies at a given key tile and shortens every wait to a few thousand polls.
+copies at a given copy unit and shortens every wait to a few thousand polls.
 The consumer's wait for the tile that never comes must give up, record
 WM_DEVERR_TIMEOUT, and let the kernel return; the next normal call must match
 the oracle.  Nothing faults or hangs: the copies that were issued are waited
@@ -90,4 +90,25 @@ def test_verify_head_dim_64_wait_times_out_then_next_call_is_clean(stall_tile):
     out, lse = wm.verify_attn(kv, q, 1.0)
     ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), [n], 1.0)
     assert_close("verify after the timeout", out, lse, ref, ref_lse)
+    assert wm.get_device_error() == 0
+
+
+@pytest.mark.parametrize("D,G,T", [(128, 4, 4), (128, 8, 4), (128, 8, 5), (256, 8, 4), (256, 8, 6)])
+@pytest.mark.parametrize("stall_unit", [0, 1, 3, 6])
+def test_tcgen05_verify_wait_times_out_then_next_call_is_clean(D, G, T, stall_unit):
+    """The tcgen05 verify kernel (16-64 rows; at head_dim 256 with more than 32
+    rows V is staged in 64-key halves by a second producer warp): the MMA
+    issuer's and the softmax warps' bounded waits give up, the kernel drains
+    its copies, frees its tensor memory and returns."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(990 + D + G + T + stall_unit)
+    B, Hkv, n = 1, 2, 1000  # 8 key tiles of 128 in one split
+    k, v = rand_bf16((B, Hkv, n, D), gen, dev), rand_bf16((B, Hkv, n, D), gen, dev)
+    kv = wm.KVCache(k, v, torch.tensor([n], device=dev))
+    q = rand_bf16((B, T, Hkv * G, D), gen, dev, 1 / math.sqrt(D))
+    _stalled(lambda: wm.verify_attn(kv, q, 1.0, n_split=1), stall_unit)
+    assert wm.get_device_error() == WM_DEVERR_TIMEOUT
+    out, lse = wm.verify_attn(kv, q, 1.0)
+    ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), [n], 1.0)
+    assert_close(f"tcgen05 verify after the timeout D={D} G={G} T={T}", out, lse, ref, ref_lse)
     assert wm.get_device_error() == 0
