@@ -50,6 +50,19 @@
 // rows over the stale ones in the staged tile before its S product, and
 // after its last tile stores them (and the tag) into the ring.  The merge
 // kernel then commits n_seen[b] = p + 1.
+//
+// Set-up that reads only kernel parameters and shared memory (the split's
+// planned key range, the barriers, the tensor-map prefetches, the L2 policy)
+// runs before griddepcontrol.wait, while the previous kernel drains.
+//
+// FMA = true (wm_set_draft_math): the same producer, stages, masks and combine
+// with both products on the CUDA cores.  Lane (k, g) of a compute warp takes
+// the logits of the warp's key k for rows 4g .. 4g + 3 (fp32 FMA over the head
+// dim, Q held as fp32 in shared memory), the row maxima over the warp's 16
+// keys come from warp shuffles, and for P.V each lane owns D/32 head-dim
+// columns of all 8 rows and reads P back from a per-warp shared buffer.  It
+// computes the same attention and is kept to measure the choice of tensor
+// cores for the draft.
 #pragma once
 
 #include <cuda_bf16.h>
