@@ -351,6 +351,7 @@ class Step:
         self.v_lse = torch.empty(inp.q_verify.shape[:3], dtype=torch.float32, device=device)
         self.d_splits = wm.plan_splits(wm.WM_OP_DRAFT_STEP, B, w.n_kv_heads, Hq, 1, D, w.slots)
         self.v_splits = wm.plan_splits(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
+        self.v_persistent = wm.verify_persistent(B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity) > 0
         dws = wm.workspace_size(wm.WM_OP_DRAFT, B, w.n_kv_heads, Hq, 1, D, w.slots)
         vws = wm.workspace_size(wm.WM_OP_VERIFY, B, w.n_kv_heads, Hq, self.T, D, self.kv.capacity)
         self.d_ws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
@@ -373,7 +374,8 @@ class Step:
 
     def launches_per_step(self, fused: bool = True) -> int:
         per_draft = 2 if fused else 2 + (1 if self.d_splits > 1 else 0)
-        return self.d * per_draft + 1 + (1 if self.v_splits > 1 else 0) + 1
+        verify = 3 if self.v_persistent else 1 + (1 if self.v_splits > 1 else 0)  # (schedule,) attention, merge
+        return self.d * per_draft + verify + 1
 
     def draft(self, j: int, fused: bool = True, q=None, k_new=None, v_new=None):
         """Draft step j: the fused step (append in the attention launch, then the merge), or ring
@@ -467,6 +469,13 @@ def workload_config(w, depth: int, context, world: int) -> dict:
     }
 
 
+def verify_schedule(st: "Step") -> str:
+    if st.v_persistent:
+        return (f"persistent: {st.v_splits} CTAs, each an equal run of the batch's key tiles (schedule made on "
+                "the device from the actual lengths), then the segment merge")
+    return f"split plan: {st.v_splits} splits per (sequence, KV head)" + (", then the merge" if st.v_splits > 1 else "")
+
+
 def step_bytes(st: "Step") -> tuple[int, int]:
     """Algorithmic HBM bytes of one verify launch and of one draft step."""
     w = st.w
@@ -527,7 +536,7 @@ def extra_1m_line(name: str, depth: int, device, flush, args, peak: float) -> di
                     "verify_frac_of_hbm": round(vg / peak, 4),
                     "draft_us_per_step": round(1e3 * draft_ms / depth, 2), "draft_gbs": round(dg, 1),
                     "draft_frac_of_hbm": round(dg / peak, 4), "draft_kv_bytes_per_step": db,
-                    "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+                    "draft_splits": st.d_splits, "verify_splits": st.v_splits, "verify_schedule": verify_schedule(st),
                     "draft_us_per_step_cuda_cores": fma_draft_chain(st, flush, args)})
     st.release()
     return out
@@ -711,7 +720,7 @@ def gpu_arm(args, rank, world, local):
                          "comes from a second capture with events between them",
             "draft_execution": "per draft step: one launch of ring append fused into the draft attention, "
                                "then the split merge (which commits the append)",
-            "draft_splits": st.d_splits, "verify_splits": st.v_splits,
+            "draft_splits": st.d_splits, "verify_splits": st.v_splits, "verify_schedule": verify_schedule(st),
             "step_us_median": round(1e3 * sorted(step_ms)[len(step_ms) // 2], 2),
             "verify_us": round(us_verify, 2),
             "verify_gbs": round(achieved, 1),

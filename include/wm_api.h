@@ -329,10 +329,30 @@ wm_status wm_draft_step(const wm_ring *ring, const wm_mem *mem, const void *k_ne
  * known here) splits are also capped at about 8 MB of K+V each, and a cap
  * that needs more than one wave is rounded up to fill its last one.  Depends
  * on the current device's SM count and the kernels' measured residency.
+ * Exception: a verify call that wm_verify_persistent accepts makes its
+ * schedule on the device; for it this returns the persistent grid's CTA count.
  * Returns 0 on invalid arguments.
  */
 int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads,
                        int32_t n_q, int32_t head_dim, int64_t max_keys, int32_t n_split);
+
+/*
+ * Whether wm_verify_attn with these arguments runs the persistent verify,
+ * and its CTA count (0: it runs the split plan).  The persistent verify
+ * serves batch > 1 at head_dim 128 (up to 64 rows per KV head, rows = n_q x
+ * n_q_heads / n_kv_heads) and 256 (up to 32 rows) when n_split = 0 and the
+ * call holds at most 2^30 key tiles of 128 (batch x n_kv_heads x
+ * ceil(max_keys / 128)).  The host sees only the largest length, so it cannot
+ * split a ragged batch evenly; the call reads the actual lengths on the
+ * device instead.  A one-CTA kernel lays the batch's key tiles end to end (the
+ * (sequence, KV head) pairs in order), and each of the grid's CTAs (as many
+ * as are resident at once) streams an equal run of them, with one partial
+ * per pair its run touches.  A merge kernel combines the partials.  Three
+ * launches per call; workspace as wm_workspace_size(WM_OP_VERIFY, ...) says.
+ * Returns 0 on invalid arguments.
+ */
+int32_t wm_verify_persistent(int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
+                             int32_t head_dim, int64_t max_keys, int32_t n_split);
 
 /*
  * Workspace bytes an attention call needs for the same arguments (0 when it

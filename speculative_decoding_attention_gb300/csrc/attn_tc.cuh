@@ -12,8 +12,8 @@
 // kept per key-thread in registers and reduced once at the end.  The shared
 // memory split between K/V staging slots and P^T buffers is chosen per head
 // dim and row count: as many staging slots as fit, then a second P^T buffer
-// if it still fits -- except 16-row tiles at head_dim 128, which take two
-// slots so that two CTAs share an SM.  Warp roles (2 + 4g warps, g = NR / 8
+// if it still fits -- except 16-row tiles at head_dim 128, which keep a short
+// ring of three slots (see tc_short_ring).  Warp roles (2 + 4g warps, g = NR / 8
 // up to 32 rows, else NR / 16):
 //   warp 0    : TMA producer -- K and V tiles (128-byte swizzle) into a ring of
 //               shared-memory slots, K_t then V_t;
@@ -94,11 +94,17 @@ struct TcLayout {
     static constexpr bool FITS = TOTAL <= 227 * 1024;
 };
 
-// Two CTAs per SM for 16-row tiles at head_dim 128: a 16-row tile has too
-// little softmax work to hide its per-tile hand-off chain, and a second CTA's
-// independent chain does (the ragged paged verify went from 56% to 87% of
-// HBM).  Each takes as many 32 KB slots as let both fit in shared memory.
-__host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 128 && nr == 16; }
+// A short staging ring (three 32 KB slots, one P^T buffer) for 16-row tiles at
+// head_dim 128 in the split-plan kernel.  It was sized for two CTAs per SM,
+// but a kernel that allocates tensor memory is resident at one CTA per SM
+// (the occupancy query answers 1 for it whatever its registers and shared
+// memory, where the same kernel without the allocation gets several), so
+// the second CTA never arrives.  At one CTA per SM the short ring still
+// measured 0-9% faster than the full one over the ragged paged mixes with
+// the split plan (many short CTAs, each filling its ring from cold), so it
+// stays there; the persistent kernel, one long run per CTA, takes the full
+// ring (SHORT = false).
+__host__ __device__ constexpr bool tc_short_ring(int d, int nr) { return d == 128 && nr == 16; }
 
 // V tiles in 64-key halves at head_dim 256 with 48 or 64 rows: the query and
 // P^T buffers leave room for only two 64 KB tile slots, so with a shared ring the
@@ -109,23 +115,21 @@ __host__ __device__ constexpr bool tc_two_per_sm(int d, int nr) { return d == 12
 // Shared-memory plan: the most K/V staging slots (up to 6) that fit with one
 // P^T buffer -- keeping enough HBM requests in flight per SM (well over 100 KB
 // at loaded HBM latency) matters most -- then a second P^T buffer if it fits.
-template <int D, int NR>
+template <int D, int NR, bool SHORT = tc_short_ring(D, NR)>
 struct TcPlan {
     static constexpr int NVS = tc_split_v(D, NR) ? 2 : 0;
     static constexpr int NSLOT = tc_split_v(D, NR) ? 1
-                                 : tc_two_per_sm(D, NR) ? (2 * TcLayout<D, NR, 3, 1>::TOTAL <= 226 * 1024 ? 3 : 2)
+                                 : SHORT ? 3
                                  : TcLayout<D, NR, 6, 1>::FITS   ? 6
                                  : TcLayout<D, NR, 5, 1>::FITS ? 5
                                  : TcLayout<D, NR, 4, 1>::FITS ? 4
                                  : TcLayout<D, NR, 3, 1>::FITS ? 3 : 2;
-    static constexpr int NPB = !tc_two_per_sm(D, NR) && TcLayout<D, NR, NSLOT, 2, NVS>::FITS ? 2 : 1;
-    static_assert(!tc_two_per_sm(D, NR) || 2 * TcLayout<D, NR, NSLOT, NPB>::TOTAL <= 228 * 1024,
-                  "two CTAs per SM must fit in shared memory");
+    static constexpr int NPB = !SHORT && TcLayout<D, NR, NSLOT, 2, NVS>::FITS ? 2 : 1;
 };
 
-template <int D, int NR>
+template <int D, int NR, bool SHORT = tc_short_ring(D, NR)>
 struct TcCfg {
-    using L = TcLayout<D, NR, TcPlan<D, NR>::NSLOT, TcPlan<D, NR>::NPB, TcPlan<D, NR>::NVS>;
+    using L = TcLayout<D, NR, TcPlan<D, NR, SHORT>::NSLOT, TcPlan<D, NR, SHORT>::NPB, TcPlan<D, NR, SHORT>::NVS>;
     static constexpr int NSLOT = L::NSLOT, NPB = L::NPB, NVS = L::NVS;
     static constexpr bool SV = NVS > 0;                        // V staged in half tiles
     static constexpr int V_OFF = L::V_OFF, VREGION = L::VREGION, VSLOT_BYTES = L::VSLOT_BYTES;
@@ -165,8 +169,10 @@ __device__ __forceinline__ bool in_smem(uint32_t lo, uint32_t len, uint32_t base
     return lo >= base && lo + len <= end;
 }
 
+// (The minimum of two blocks for the short-ring instance only caps its
+// registers, at the 95 it was measured with.)
 template <int D, int NR>
-__global__ void __launch_bounds__(tc_threads(D, NR), tc_two_per_sm(D, NR) ? 2 : 1)
+__global__ void __launch_bounds__(tc_threads(D, NR), tc_short_ring(D, NR) ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const AttnParams p) {
     using C = TcCfg<D, NR>;

@@ -240,6 +240,52 @@ size_t partial_bytes(int64_t rows_total, int n_split, int head_dim) {
     return o_aligned + (size_t)rows_total * n_split * sizeof(float);
 }
 
+// The persistent verify (attn_tcp.cuh) serves a batch of several sequences on
+// the tcgen05 kernel when the caller leaves the split count to the library:
+// it reads the actual lengths on the device and gives every resident CTA the
+// same number of key tiles.  Returns its CTA count, or 0 when the call runs
+// the split plan instead (one sequence, an explicit n_split, a configuration
+// with half-tile V staging, or more than 2^30 key tiles per call, which keeps
+// every tile count of the schedule within 32 bits).
+int tcp_ctas(int op, int batch, int n_kv_heads, int rows, int head_dim, int64_t max_keys, int n_split) {
+    const int nr = 16 * ((rows + 15) / 16);
+    if (op != WM_OP_VERIFY || !use_tc_kernel(op, head_dim) || batch <= 1 || n_split != 0 ||
+        !tcp_supported(head_dim, nr))
+        return 0;
+    const int64_t tiles = (max_keys + kTcTile - 1) / kTcTile;
+    if ((int64_t)batch * n_kv_heads * tiles > (int64_t)1 << 30) return 0;
+    static std::mutex mu;
+    static int cache[kMaxDevices][2][4] = {};
+    int dev = 0;
+    int per_sm = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(mu);
+        int &n = cache[dev][head_dim == 128 ? 0 : 1][nr / 16 - 1];
+        if (!n) n = std::max(1, head_dim == 128 ? attn_tcp_blocks_per_sm_d128(nr) : attn_tcp_blocks_per_sm_d256(nr));
+        per_sm = n;
+    }
+    const int sms = sm_count();
+    return per_sm * (sms > 0 ? sms : 1);
+}
+
+// Workspace of the persistent verify: segment partials (n_cta + units - 1
+// segments of `rows` rows), the schedule (chunk, total, tile prefix) and the
+// CTAs' first tiles, each part 256-byte aligned.
+struct TcpLayout {
+    size_t o = 0, lse = 0, sched = 0, start = 0, total = 0;
+};
+TcpLayout tcp_layout(int n_cta, int64_t units, int rows, int head_dim, int batch) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t n_seg = (size_t)n_cta + (size_t)units - 1;
+    TcpLayout l;
+    l.o = 0;
+    l.lse = up(n_seg * rows * head_dim * sizeof(float));
+    l.sched = l.lse + up(n_seg * rows * sizeof(float));
+    l.start = l.sched + up(((size_t)batch + 3) * sizeof(int64_t));
+    l.total = l.start + (size_t)n_cta * sizeof(int4);
+    return l;
+}
+
 // maps: K and V of the cache or ring, then K and V of the memory-slot store
 // (the same two again when there is none).
 cudaError_t launch_attn_any(int op, const CUtensorMap (&maps)[4], const AttnParams &p, bool step,
@@ -358,15 +404,30 @@ int32_t wm_plan_splits(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_
         op = WM_OP_DRAFT;  // all draft forms split alike
     }
     const int rows = n_q * (n_q_heads / n_kv_heads);
+    const int n_cta = tcp_ctas(op, batch, n_kv_heads, rows, head_dim, max_keys, n_split);
+    if (n_cta > 0) return n_cta;
     return plan_splits(batch * n_kv_heads, batch, max_keys, n_split, key_tile(op, head_dim), head_dim,
                        ctas_per_sm(op, head_dim, rows), use_draft_kernel(op, rows))
         .n_split;
+}
+
+int32_t wm_verify_persistent(int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q, int32_t head_dim,
+                             int64_t max_keys, int32_t n_split) {
+    if (batch <= 0 || n_kv_heads <= 0 || n_q_heads <= 0 || n_q <= 0 || n_q_heads % n_kv_heads ||
+        !head_dim_ok(head_dim) || max_keys < 0 || n_split < 0)
+        return 0;
+    return tcp_ctas(WM_OP_VERIFY, batch, n_kv_heads, n_q * (n_q_heads / n_kv_heads), head_dim, max_keys, n_split);
 }
 
 size_t wm_workspace_size(int32_t op, int32_t batch, int32_t n_kv_heads, int32_t n_q_heads, int32_t n_q,
                          int32_t head_dim, int64_t max_keys, int32_t n_split) {
     const int32_t ns = wm_plan_splits(op, batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split);
     if (ns <= 0) return (size_t)-1;
+    if (n_q_heads % n_kv_heads == 0) {
+        const int rows = n_q * (n_q_heads / n_kv_heads);
+        const int n_cta = tcp_ctas(op, batch, n_kv_heads, rows, head_dim, max_keys, n_split);
+        if (n_cta > 0) return tcp_layout(n_cta, (int64_t)batch * n_kv_heads, rows, head_dim, batch).total;
+    }
     if (op == WM_OP_DRAFT_STEP || op == WM_OP_DRAFT_MEM)  // partials even when unsplit (fused step)
         return partial_bytes((int64_t)batch * n_q_heads, ns, head_dim);
     if (ns == 1) return 0;
@@ -453,6 +514,39 @@ static wm_status run_attention(int op, AttnParams &p, const MapEncoder &encode_m
                                int64_t *commit_n_seen = nullptr) {
     const bool step = commit_n_seen != nullptr;
     if ((int64_t)p.batch * p.n_kv_heads > kMaxUnits) return WM_ERR_UNSUPPORTED;
+    const int n_cta = step ? 0 : tcp_ctas(op, p.batch, p.n_kv_heads, p.rows, p.head_dim, max_keys, n_split);
+    if (n_cta > 0) {
+        // persistent verify: schedule (one CTA), the verify grid, the segment merge
+        const TcpLayout l = tcp_layout(n_cta, (int64_t)p.batch * p.n_kv_heads, p.rows, p.head_dim, p.batch);
+        if (!ws || ws_bytes < l.total || !aligned(ws, 256)) return WM_ERR_WORKSPACE;
+        char *w = static_cast<char *>(ws);
+        int64_t *sched = reinterpret_cast<int64_t *>(w + l.sched);
+        int4 *cta_start = reinterpret_cast<int4 *>(w + l.start);
+        p.n_split = n_cta;
+        p.keys_per_split = 0;
+        p.out = out;
+        p.lse = lse;
+        p.o_part = reinterpret_cast<float *>(w + l.o);
+        p.lse_part = reinterpret_cast<float *>(w + l.lse);
+        p.tile_prefix = sched + 2;
+        p.cta_start = cta_start;
+        p.err = device_error_ptr();
+        if (!p.err) return WM_ERR_CUDA;
+        p.wait_limit = t_wait_limit;
+        p.stall_tile = t_stall_tile;
+        CUtensorMap maps[4];
+        if (!encode_maps(maps)) return WM_ERR_CUDA;
+        const int nr = 16 * ((p.rows + 15) / 16);
+        cudaError_t e = launch_verify_sched(p.seq_lens, p.batch, p.n_kv_heads, p.capacity, n_cta, sched, cta_start,
+                                            p.err, st);
+        if (e != cudaSuccess) return WM_ERR_CUDA;
+        e = p.head_dim == 128 ? launch_attn_tcp_d128(maps[0], maps[1], p, nr, n_cta, st)
+                              : launch_attn_tcp_d256(maps[0], maps[1], p, nr, n_cta, st);
+        if (e != cudaSuccess) return WM_ERR_CUDA;
+        e = launch_seg_merge(p.o_part, p.lse_part, sched, p.batch, p.n_kv_heads, p.n_q, p.n_q_heads, p.head_dim, out,
+                             lse, st);
+        return e == cudaSuccess ? WM_OK : WM_ERR_CUDA;
+    }
     const bool keys_as_m = use_draft_kernel(op, p.rows);
     const SplitPlan pl = plan_splits(p.batch * p.n_kv_heads, p.batch, max_keys, n_split, key_tile(op, p.head_dim),
                                      p.head_dim, ctas_per_sm(op, p.head_dim, p.rows), keys_as_m);

@@ -83,6 +83,11 @@ struct AttnParams {
     // keys-as-M draft kernel only: balanced splits of the plan's key tiles
     // (plan_tiles = q * n_split + r: the first r splits take q + 1 tiles, the rest q)
     int32_t plan_tiles;
+    // persistent tcgen05 verify over a batch (device-side schedule, verify_sched.cu):
+    // tiles of one KV head before each sequence ([batch + 1]) and each CTA's run;
+    // its partials are o_part [segments][rows][D] and lse_part [segments][rows]
+    const int64_t *tile_prefix;
+    const int4 *cta_start;  // [grid]: (sequence, KV head, first tile in that unit, tiles)
 };
 
 // Launch the attention kernel for head dim D (defined in attn_d<D>.cu).  mk/mv
@@ -135,6 +140,30 @@ constexpr int kTcTile = 128;
 // Resident CTAs per SM of the tcgen05 kernel for n_rows16 rows (0 if unknown).
 int attn_tc_blocks_per_sm_d128(int n_rows16);
 int attn_tc_blocks_per_sm_d256(int n_rows16);
+
+// Persistent tcgen05 verify for a batch of sequences (attn_tcp_d<D>.cu): n_cta
+// CTAs, each streaming the run of key tiles the schedule gives it.  Not
+// instantiated for the configurations that stage V in half tiles (head_dim
+// 256 with more than 32 rows): tcp_supported says which are.
+__host__ __device__ constexpr bool tcp_supported(int head_dim, int n_rows16) {
+    return (head_dim == 128 || head_dim == 256) && n_rows16 >= 16 && n_rows16 <= 64 && n_rows16 % 16 == 0 &&
+           !(head_dim == 256 && n_rows16 >= 48);
+}
+cudaError_t launch_attn_tcp_d128(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int n_rows16,
+                                 int n_cta, cudaStream_t stream);
+cudaError_t launch_attn_tcp_d256(const CUtensorMap &k, const CUtensorMap &v, const AttnParams &p, int n_rows16,
+                                 int n_cta, cudaStream_t stream);
+int attn_tcp_blocks_per_sm_d128(int n_rows16);
+int attn_tcp_blocks_per_sm_d256(int n_rows16);
+
+// The schedule of the persistent verify (verify_sched.cu): sched [batch + 3]
+// int64 (chunk, total tiles, tile prefix [batch + 1]) and cta_start [n_cta];
+// and the merge of its segment partials into out / lse_out.
+cudaError_t launch_verify_sched(const int64_t *seq_lens, int batch, int n_kv_heads, int64_t capacity, int n_cta,
+                                int64_t *sched, int4 *cta_start, int32_t *err, cudaStream_t stream);
+cudaError_t launch_seg_merge(const float *o_seg, const float *lse_seg, const int64_t *sched, int batch,
+                             int n_kv_heads, int n_q, int n_q_heads, int head_dim, void *out, float *lse_out,
+                             cudaStream_t stream);
 
 // Ring and merge kernels (ring.cu, merge.cu).
 cudaError_t launch_ring_append(void *rk, void *rv, int32_t *tag, int64_t *n_seen, int batch,

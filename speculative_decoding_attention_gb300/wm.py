@@ -22,7 +22,7 @@ WM_DRAFT_MATH_MMA, WM_DRAFT_MATH_FMA = 0, 1
 DEVERR_NAMES = {0: "none", 1: "bad length", 2: "bad page", 3: "pipeline wait timeout", 4: "internal check"}
 
 EXPORTED = ("wm_ring_append", "wm_ring_fill", "wm_ring_rollback", "wm_draft_attn", "wm_verify_attn",
-            "wm_lse_merge", "wm_plan_splits", "wm_workspace_size", "wm_get_device_error",
+            "wm_lse_merge", "wm_plan_splits", "wm_verify_persistent", "wm_workspace_size", "wm_get_device_error",
             "wm_status_string", "wm_version", "wm_draft_attn_static", "wm_draft_step", "wm_draft_attn_mem",
             "wm_mem_append", "wm_mem_rollback", "wm_set_test_stall", "wm_set_draft_math")
 STATIC_SCRATCH_BYTES = 8 << 20  # WM_STATIC_SCRATCH_BYTES
@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.wm_lse_merge.argtypes = [P, P, I32, I64, I32, P, P, P]
         lib.wm_plan_splits.argtypes = [I32, I32, I32, I32, I32, I32, I64, I32]
         lib.wm_plan_splits.restype = I32
+        lib.wm_verify_persistent.argtypes = [I32, I32, I32, I32, I32, I64, I32]
+        lib.wm_verify_persistent.restype = I32
         lib.wm_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I64, I32]
         lib.wm_workspace_size.restype = ctypes.c_size_t
         lib.wm_get_device_error.argtypes = [ctypes.POINTER(I32), P]
@@ -280,6 +282,13 @@ def ring_rollback(ring: Ring, new_len: torch.Tensor, stream=None) -> None:
 def plan_splits(op: int, batch: int, n_kv_heads: int, n_q_heads: int, n_q: int, head_dim: int,
                 max_keys: int, n_split: int = 0) -> int:
     return int(load().wm_plan_splits(op, batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split))
+
+
+def verify_persistent(batch: int, n_kv_heads: int, n_q_heads: int, n_q: int, head_dim: int, max_keys: int,
+                      n_split: int = 0) -> int:
+    """CTA count of the persistent verify for these arguments, 0 when the call
+    runs the split plan (see wm_verify_persistent in include/wm_api.h)."""
+    return int(load().wm_verify_persistent(batch, n_kv_heads, n_q_heads, n_q, head_dim, max_keys, n_split))
 
 
 def workspace_size(op: int, batch: int, n_kv_heads: int, n_q_heads: int, n_q: int, head_dim: int,

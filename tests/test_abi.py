@@ -296,3 +296,42 @@ def test_draft_math_setting(lib):
     assert lib.wm_set_draft_math(-1) == wm.WM_ERR_INVALID_ARG
     assert lib.wm_set_draft_math(wm.WM_DRAFT_MATH_FMA) == wm.WM_OK
     assert lib.wm_set_draft_math(wm.WM_DRAFT_MATH_MMA) == wm.WM_OK
+
+
+def test_verify_persistent_selection(lib):
+    """The persistent verify serves batches of several sequences left to the
+    library at head_dim 128 (<= 64 rows) and 256 (<= 32 rows), up to 2^30 key
+    tiles per call; everything else runs the split plan.  Without a device the
+    CTA count is one per SM of an unknown device: 1."""
+    vp = wm.verify_persistent
+    assert vp(2, 2, 8, 3, 128, 4096) > 0
+    assert vp(2, 8, 64, 8, 128, 4096) > 0      # 64 rows
+    assert vp(2, 2, 16, 4, 256, 4096) > 0      # 32 rows at head_dim 256
+    assert vp(2, 2, 16, 5, 256, 4096) == 0     # 40 rows at head_dim 256: V in half tiles
+    assert vp(1, 2, 8, 3, 128, 4096) == 0      # one sequence: the split plan is balanced already
+    assert vp(2, 2, 8, 3, 128, 4096, 4) == 0   # explicit split count
+    assert vp(2, 2, 8, 3, 64, 4096) == 0       # head_dim 64: mma.sync kernel
+    assert vp(4, 8, 32, 3, 128, 1 << 25) > 0   # 4 x 8 x 2^18 = 2^23 key tiles
+    assert vp(4096, 16, 64, 3, 128, 1 << 31) == 0  # 2^12 x 2^4 x 2^24 tiles > 2^30
+    assert vp(2, 3, 8, 3, 128, 4096) == 0      # n_q_heads not a multiple of n_kv_heads
+    assert vp(0, 2, 8, 3, 128, 4096) == 0
+
+
+def test_verify_persistent_workspace_layout(lib):
+    """Workspace of the persistent verify: partials of n_cta + units - 1
+    segments (rows x head_dim fp32, then rows fp32), the schedule (batch + 3
+    int64) and the CTAs' first tiles (16 bytes each), each part 256-byte
+    aligned, and WM_ERR_WORKSPACE one byte short."""
+    up = lambda x: (x + 255) // 256 * 256
+    B, Hkv, G, T, D = 5, 2, 4, 3, 128
+    n_cta = wm.verify_persistent(B, Hkv, Hkv * G, T, D, 4096)
+    assert n_cta >= 1
+    assert wm.plan_splits(wm.WM_OP_VERIFY, B, Hkv, Hkv * G, T, D, 4096, 0) == n_cta
+    rows, seg = T * G, n_cta + B * Hkv - 1
+    want = up(seg * rows * D * 4) + up(seg * rows * 4) + up((B + 3) * 8) + n_cta * 16
+    need = wm.workspace_size(wm.WM_OP_VERIFY, B, Hkv, Hkv * G, T, D, 4096, 0)
+    assert need == want
+    P = ctypes.c_void_p
+    s = _kv(batch=B, n_kv_heads=Hkv)
+    assert lib.wm_verify_attn(ctypes.byref(s), P(1 << 24), T, Hkv * G, 1.0, 0, P(1 << 25), None, P(1 << 26),
+                              need - 1, None) == wm.WM_ERR_WORKSPACE

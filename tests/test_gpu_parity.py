@@ -317,17 +317,19 @@ def test_lse_merge_kernel_matches_oracle():
 
 def test_split_plan_fills_waves():
     """Default plans: one wave of resident CTAs for a single sequence; for a
-    batch, the per-split K+V cap rounded up to fill its last wave."""
+    batch on the split plan, the per-split K+V cap rounded up to fill its last
+    wave."""
     gpu()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # hybrid verify: 2 KV heads, 32 rows at head_dim 256 (one CTA per SM), 1M keys
     assert wm.plan_splits(wm.WM_OP_VERIFY, 1, 2, 16, 4, 256, 1 << 20, 0) == sms // 2
-    # two 1M sequences x 8 KV heads, 40 rows at head_dim 128 (one CTA per SM):
-    # the 8 MB cap asks for ceil(1M / 16384) = 64 splits, 1024 CTAs; the count
-    # is raised to the most splits that still fit in ceil(1024 / sms) waves
-    ns = wm.plan_splits(wm.WM_OP_VERIFY, 2, 8, 64, 5, 128, 1 << 20, 0)
-    units, waves = 16, -(-16 * 64 // sms)
-    assert ns >= 64 and units * ns <= waves * sms < units * (ns + 1)
+    # two 1M sequences x 8 KV heads, 40 rows at head_dim 256 (V in half tiles,
+    # so the split plan rather than the persistent grid; one CTA per SM): the
+    # 8 MB cap asks for ceil(1M / 8192) = 128 splits, 2048 CTAs; the count is
+    # raised to the most splits that still fit in ceil(2048 / sms) waves
+    ns = wm.plan_splits(wm.WM_OP_VERIFY, 2, 8, 64, 5, 256, 1 << 20, 0)
+    units, waves = 16, -(-16 * 128 // sms)
+    assert ns >= 128 and units * ns <= waves * sms < units * (ns + 1)
 
 
 @pytest.mark.parametrize("B,cap,paged", [(3, 20000, False), (16, 6000, True), (17, 3000, False)])
