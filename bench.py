@@ -43,7 +43,7 @@ METRIC = "decode-attn µs/step & HBM GB/s (% roofline): windowed draft vs full v
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
-KERNEL_SOURCES = ("attn_tc.cuh", "tc.cuh", "ptx.cuh", "wm_internal.h")
+KERNEL_SOURCES = ("attn_tc.cuh", "attn_tcp.cuh", "tc.cuh", "ptx.cuh", "wm_internal.h")
 
 
 def parse():
@@ -751,7 +751,8 @@ def gpu_arm(args, rank, world, local):
             "other_1m_configs": others or None,
         },
         "roofline": {
-            "kernel": "attn_tc_kernel (tcgen05 verify, split-KV) + lse_merge",
+            "kernel": ("verify_sched + attn_tcp_kernel (persistent tcgen05 verify) + seg_merge" if st.v_persistent
+                       else "attn_tc_kernel (tcgen05 verify, split-KV) + lse_merge"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
