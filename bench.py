@@ -508,6 +508,53 @@ def time_graph(graph, flush, n_warm: int, n: int, ev=None):
     return ms
 
 
+def graph_ms(st: "Step", fn, flush, args, n=None) -> float:
+    """Mean milliseconds of ``fn`` captured as a graph of its own: the L2
+    flushed before every replay (pass ``flush=lambda: None`` to keep it warm),
+    CUDA events on the stream around the replay."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=st.dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    ms = time_graph(g, flush, max(3, args.warmup), n or args.steps)
+    return sum(ms) / len(ms)
+
+
+def parts(st: "Step", flush, args) -> dict:
+    """The draft chain and the verify, each timed as a graph of its own, the
+    way the step is (``graph_ms``).  Each graph ends with the ring rollback
+    that resets the ring for the next replay, so a graph holding only that
+    rollback is timed too and subtracted (it also carries the graph launch's
+    own fixed cost); the other draft chains below are timed the same way.
+    The draft graph is also replayed without the flush: the ring stays in L2
+    from one replay to the next, as in a decode loop.  Milliseconds."""
+    wm, w, inp = st.wm, st.w, st.inp
+
+    def rollback():
+        wm.ring_rollback(st.ring, st.base_len)
+
+    def drafts():
+        for j in range(st.d):
+            st.draft(j)
+        rollback()
+
+    def verify():
+        wm.verify_attn(st.kv, inp.q_verify, w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
+        rollback()
+
+    no_flush = lambda: None
+    st.rollback_graph_ms = graph_ms(st, rollback, flush, args)
+    d_graph, v_graph = graph_ms(st, drafts, flush, args), graph_ms(st, verify, flush, args)
+    return {"draft_ms": d_graph - st.rollback_graph_ms, "verify_ms": v_graph - st.rollback_graph_ms,
+            "draft_graph_ms": d_graph, "verify_graph_ms": v_graph,
+            "draft_warm_ms": graph_ms(st, drafts, no_flush, args) - graph_ms(st, rollback, no_flush, args),
+            "rollback_graph_ms": st.rollback_graph_ms}
+
+
 def breakdown(st: "Step", flush, args) -> tuple[float, float]:
     """Mean draft-chain and verify milliseconds from a capture of the step with
     events between them (the events cost time themselves, so this graph is never
@@ -526,7 +573,8 @@ def extra_1m_line(name: str, depth: int, device, flush, args, peak: float) -> di
     st = Step(w, depth, device)
     st.capture(events=False)
     step_ms = time_graph(st.graph, flush, max(3, args.warmup), args.steps)
-    draft_ms, verify_ms = breakdown(st, flush, args)
+    pt = parts(st, flush, args)
+    draft_ms, verify_ms = pt["draft_ms"], pt["verify_ms"]
     vb, db = step_bytes(st)
     out = {"step_us": round(1e3 * sum(step_ms) / len(step_ms), 2)}
     if verify_ms:
@@ -640,26 +688,11 @@ def gpu_arm(args, rank, world, local):
         clk.mark(t_begin, t_end)
         clk.load_until_sampled(untimed_step, 2)
     clocks = clk.summary()
-    draft_ms, verify_ms = breakdown(st, flush, args)
-    # The same step graph replayed without the flush: the ring stays in L2
-    # from one step to the next (the verify streams its cache evict-first).
-    warm_draft_ms = []
-    if st.ev:
-        for i in range(3 + max(3, args.steps // 2)):
-            st.graph.replay()
-            torch.cuda.synchronize()
-            if i >= 3:
-                warm_draft_ms.append(st.ev[0].elapsed_time(st.ev[1]))
-    if not st.ev:  # no in-graph events: time the verify alone, same way
-        vms = []
-        for _ in range(args.steps):
-            flush()
-            e0.record()
-            wm.verify_attn(st.kv, st.inp.q_verify, w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
-            e1.record()
-            e1.synchronize()
-            vms.append(e0.elapsed_time(e1))
-        verify_ms = sum(vms) / len(vms)
+    pt = parts(st, flush, args)
+    draft_ms, verify_ms = pt["draft_ms"], pt["verify_ms"]
+    # Cross-check: the step captured with events between its draft chain and
+    # its verify (the event nodes cost time themselves).
+    ev_draft_ms, ev_verify_ms = breakdown(st, flush, args)
     if wm.get_device_error():
         raise RuntimeError("device error during the timed steps")
     out_ok = bool(torch.isfinite(st.v_out.float()).all() and torch.isfinite(st.d_out.float()).all())
@@ -716,8 +749,10 @@ def gpu_arm(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) K/V and queries in the workload's shapes; no dataset)",
         "config": config,
         "detail": {
-            "execution": "one CUDA graph per step holding the step's kernels only; the draft / verify breakdown "
-                         "comes from a second capture with events between them",
+            "execution": "one CUDA graph per step holding the step's kernels only; the draft and verify figures "
+                         "time the draft chain and the verify each as a graph of its own (L2 flushed before every "
+                         "replay, events on the stream around it), each ending with the ring rollback, minus a "
+                         "graph holding only that rollback",
             "draft_execution": "per draft step: one launch of ring append fused into the draft attention, "
                                "then the split merge (which commits the append)",
             "draft_splits": st.d_splits, "verify_splits": st.v_splits, "verify_schedule": verify_schedule(st),
@@ -731,10 +766,19 @@ def gpu_arm(args, rank, world, local):
             "draft_kv_bytes_per_step": 2 * B * Hkv * w.slots * D * 2,
             "draft_l2": "L2 flushed before each step; draft steps 2..d re-read the ring (S+W slots) "
                         "mostly from L2, as a decode loop does",
-            "draft_us_per_step_warm_l2": (round(1e3 * sum(warm_draft_ms) / len(warm_draft_ms) / depth, 2)
-                                          if warm_draft_ms else None),
-            "draft_warm_l2": "the same step graph replayed without the flush: the ring stays in L2 from step "
-                             "to step (the verify reads its cache evict-first)",
+            "draft_us_per_step_warm_l2": round(1e3 * pt["draft_warm_ms"] / depth, 2),
+            "draft_warm_l2": "the draft chain's graph replayed without the flush: the ring stays in L2 from "
+                             "replay to replay",
+            "rollback_graph_us": round(1e3 * pt["rollback_graph_ms"], 2),
+            "marginal_in_step": {"draft_us_per_step": round((us_step - 1e3 * pt["verify_graph_ms"]) / depth, 2),
+                                 "verify_us": round(us_step - 1e3 * pt["draft_graph_ms"], 2),
+                                 "note": "what each part adds to the whole step: the step minus the graph of the "
+                                         "verify (with the rollback), and minus the graph of the draft chain (with "
+                                         "the rollback)"},
+            "in_graph_events": {"draft_us_per_step": None if ev_draft_ms is None else round(1e3 * ev_draft_ms / depth, 2),
+                                "verify_us": None if ev_verify_ms is None else round(1e3 * ev_verify_ms, 2),
+                                "note": "the same split from one capture of the whole step with events between its "
+                                        "draft chain and its verify; the event nodes cost time themselves"},
             "draft_launch_floor_us": floors,
             "unfused_draft_us_per_step": None if unfused_ms is None else round(1e3 * unfused_ms / depth, 2),
             "draft_us_per_step_cuda_cores": fma_us,
@@ -772,56 +816,35 @@ def gpu_arm(args, rank, world, local):
 def fma_draft_chain(st: Step, flush, args):
     """The fused draft chain with the draft kernel's products on the CUDA cores
     (fp32 FMA, warp-shuffle softmax) instead of mma.sync: the measurement behind
-    the choice of tensor cores for the draft.  Mean us per draft step (in-graph
-    events around the chain, L2 flushed before each replay), or None without
-    in-graph events."""
+    the choice of tensor cores for the draft.  Mean us per draft step, timed as
+    the draft chain of ``parts`` is."""
     wm, w, inp = st.wm, st.w, st.inp
     wm.set_draft_math(wm.WM_DRAFT_MATH_FMA)
     try:
         ws = wm.step_workspace(st.ring, w.n_q_heads)
 
-        def chain(ev=None):
-            if ev:
-                ev[0].record()
+        def chain():
             for j in range(st.d):
                 wm.draft_step(st.ring, inp.k_new[j], inp.v_new[j], inp.q_draft[j], w.scale, ws, out=st.d_out[j],
                               lse=st.d_lse[j])
-            if ev:
-                ev[1].record()
             wm.ring_rollback(st.ring, st.base_len)
 
-        chain()
-        torch.cuda.synchronize()
-        try:
-            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-        except TypeError:
-            return None
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device=st.dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(g, stream=s):
-            chain(ev)
-        ms = time_graph(g, flush, max(3, args.warmup), max(3, args.steps // 2), ev=ev)
+        ms = graph_ms(st, chain, flush, args, n=max(3, args.steps // 2)) - st.rollback_graph_ms
     finally:
         wm.set_draft_math(wm.WM_DRAFT_MATH_MMA)
-    return round(1e3 * sum(m[0] for m in ms) / len(ms) / st.d, 2)
+    return round(1e3 * ms / st.d, 2)
 
 
 def unfused_draft_chain(st: Step, flush, args):
     """The draft chain as three launches per draft step (ring append, draft
-    attention, split merge): the whole step captured with in-graph events,
-    the draft interval averaged.  None without in-graph events."""
-    graph, ev = st.capture(fused=False)
-    if not ev:
-        return None
-    ms = []
-    for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
-        flush()
-        graph.replay()
-        torch.cuda.synchronize()
-        if i >= max(3, args.warmup):
-            ms.append(ev[0].elapsed_time(ev[1]))
-    return sum(ms) / len(ms)
+    attention, split merge), timed as the draft chain of ``parts`` is.  Mean
+    milliseconds per chain."""
+    def chain():
+        for j in range(st.d):
+            st.draft(j, fused=False)
+        st.wm.ring_rollback(st.ring, st.base_len)
+
+    return graph_ms(st, chain, flush, args, n=max(3, args.steps // 2)) - st.rollback_graph_ms
 
 
 MASW_SLOT_INTERVAL = 256  # one memory slot per 256 tokens of history
@@ -831,7 +854,7 @@ def masw_draft_chain(st: Step, flush, args):
     """The draft chain with memory slots (memory-augmented sliding window): the
     fused step over sinks + window + one materialized slot per
     MASW_SLOT_INTERVAL tokens of each sequence's history (synthetic slot K/V),
-    captured with in-graph events.  None without in-graph events."""
+    timed as the draft chain of ``parts`` is."""
     wm, w, inp = st.wm, st.w, st.inp
     B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
     counts = [n // MASW_SLOT_INTERVAL for n in inp.seq_lens_host]
@@ -843,35 +866,13 @@ def masw_draft_chain(st: Step, flush, args):
     mem.count.copy_(torch.tensor(counts, dtype=torch.int64, device=st.dev))
     ws = wm.step_workspace(st.ring, Hq, mem=mem)
 
-    def chain(ev=None):
-        if ev:
-            ev[0].record()
+    def chain():
         for j in range(st.d):
             wm.draft_step(st.ring, inp.k_new[j], inp.v_new[j], inp.q_draft[j], w.scale, ws, out=st.d_out[j],
                           lse=st.d_lse[j], mem=mem)
-        if ev:
-            ev[1].record()
         wm.ring_rollback(st.ring, st.base_len)
 
-    chain()
-    torch.cuda.synchronize()
-    try:
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-    except TypeError:
-        return None
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(device=st.dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(g, stream=s):
-        chain(ev)
-    ms = []
-    for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
-        flush()
-        g.replay()
-        torch.cuda.synchronize()
-        if i >= max(3, args.warmup):
-            ms.append(ev[0].elapsed_time(ev[1]))
-    us = 1e3 * sum(ms) / len(ms) / st.d
+    us = 1e3 * (graph_ms(st, chain, flush, args, n=max(3, args.steps // 2)) - st.rollback_graph_ms) / st.d
     kv_bytes = 2 * Hkv * D * 2 * sum(w.slots + c for c in counts)
     return {"slot_interval": MASW_SLOT_INTERVAL, "slots": counts, "us_per_step": round(us, 2),
             "kv_bytes_per_step": kv_bytes, "gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1)}
@@ -882,7 +883,8 @@ def native_draft_chain(st: Step, flush, args) -> tuple[float, float]:
     against): each of the d draft steps attends over the whole cache, i.e. the
     verify kernel with one query position over positions 0..N_b+j.  Returns the
     mean milliseconds per chain and per native step (the chain followed by the
-    verify), each graph-captured with the L2 flushed between replays."""
+    verify and the rollback, like the windowed step), each graph-captured with
+    the L2 flushed between replays."""
     wm, w, inp = st.wm, st.w, st.inp
     B, Hq, D = w.batch, w.n_q_heads, w.head_dim
     lens = [torch.tensor([n + j + 1 for n in inp.seq_lens_host], dtype=torch.int64, device=st.dev)
@@ -897,33 +899,17 @@ def native_draft_chain(st: Step, flush, args) -> tuple[float, float]:
     def chain():
         for j in range(st.d):
             wm.verify_attn(kvs[j], qs[j], w.scale, out=out, lse=lse, workspace=ws)
+        wm.ring_rollback(st.ring, st.base_len)  # as in the windowed chain's graph (a no-op here)
 
-    def step():  # the native step: the draft chain, then the same verify as the windowed step
-        chain()
+    def step():  # the native step: the draft chain, then the same verify as the windowed step, then the rollback
+        for j in range(st.d):
+            wm.verify_attn(kvs[j], qs[j], w.scale, out=out, lse=lse, workspace=ws)
         wm.verify_attn(st.kv, inp.q_verify, w.scale, out=st.v_out, lse=st.v_lse, workspace=st.v_ws)
+        wm.ring_rollback(st.ring, st.base_len)
 
-    def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device=st.dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(g, stream=s):
-            fn()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        ms = []
-        for i in range(max(3, args.warmup) + max(3, args.steps // 2)):
-            flush()
-            e0.record()
-            g.replay()
-            e1.record()
-            e1.synchronize()
-            if i >= max(3, args.warmup):
-                ms.append(e0.elapsed_time(e1))
-        return sum(ms) / len(ms)
-
-    return timed(chain), timed(step)
+    # the chain as the windowed chain is timed; the step as the windowed step is
+    n = max(3, args.steps // 2)
+    return graph_ms(st, chain, flush, args, n=n) - st.rollback_graph_ms, graph_ms(st, step, flush, args, n=n)
 
 
 def _packed(specs, device, pinned: bool):
