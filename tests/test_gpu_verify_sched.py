@@ -72,6 +72,14 @@ def test_many_short_sequences(paged):
     check(f"300 short sequences paged={paged}", lens, 2, 4, 2, 128, paged, 1201 + paged)
 
 
+def test_batch_beyond_the_shared_memory_prefix():
+    """More sequences than the schedule keeps in shared memory (2048): its
+    searches read the tile prefix back from global memory."""
+    g = torch.Generator().manual_seed(1250)
+    lens = torch.randint(0, 300, (2100,), generator=g).tolist()
+    check("2100 sequences", lens, 1, 4, 1, 128, False, 1251)
+
+
 def test_one_long_sequence_among_tiny_ones():
     """The first runs cross dozens of tiny units before reaching the long one,
     whose tiles are shared by most of the grid."""
