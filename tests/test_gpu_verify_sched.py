@@ -196,3 +196,44 @@ def test_persistent_wait_times_out_then_next_call_is_clean(D, G, T, stall_unit):
     ref, ref_lse = oracle.verify(oracle_kv(k, v), q.cpu(), lens, 1.0)
     assert_close(f"persistent verify after the timeout D={D} G={G} T={T}", out, lse, ref, ref_lse)
     assert wm.get_device_error() == 0
+
+
+@pytest.mark.parametrize("D,G,T,paged", [(128, 4, 3, True), (128, 8, 5, False), (256, 8, 4, False)])
+def test_many_graph_replays_are_bit_identical(D, G, T, paged):
+    """300 replays of a captured persistent verify over a mix whose runs cross
+    several units (segment boundaries, query restaging, partial slots): every
+    replay gives the first replay's bits, and the first matches the oracle --
+    a race on a barrier phase or a buffer would show as a differing replay."""
+    dev = gpu()
+    gen = torch.Generator(device=dev).manual_seed(2100 + D + G + T)
+    lens = [3000, 17, 2500, 0, 129, 4100, 640, 1]
+    Hkv = 2
+    k, v, bt = make_cache(lens, Hkv, D, gen, dev, paged, seed=2101)
+    kv = wm.KVCache(k, v, torch.tensor(lens, dtype=torch.int64, device=dev), bt)
+    q = rand_bf16((len(lens), T, Hkv * G, D), gen, dev, 1 / math.sqrt(D))
+    need = wm.workspace_size(wm.WM_OP_VERIFY, len(lens), Hkv, Hkv * G, T, D, kv.capacity)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = torch.empty((len(lens), T, Hkv * G, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((len(lens), T, Hkv * G), dtype=torch.float32, device=dev)
+    wm.verify_attn(kv, q, 1.0, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    graph, s = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=s):
+        wm.verify_attn(kv, q, 1.0, out=out, lse=lse, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    ref, r_lse = oracle.verify(oracle_kv(k, v, bt), q.cpu(), lens, 1.0)
+    assert_close(f"persistent D={D} rows={G * T}", ref_out, ref_lse, ref, r_lse)
+    outs = torch.empty((300,) + out.shape, dtype=out.dtype, device=dev)
+    lses = torch.empty((300,) + lse.shape, dtype=lse.dtype, device=dev)
+    for i in range(300):
+        out.fill_(float("nan"))
+        graph.replay()
+        outs[i].copy_(out)
+        lses[i].copy_(lse)
+    torch.cuda.synchronize()
+    same = [(torch.equal(outs[i], ref_out) and torch.equal(lses[i], ref_lse)) for i in range(300)]
+    assert all(same), f"{same.count(False)} of 300 replays differ from the first"
+    assert wm.get_device_error() == 0
