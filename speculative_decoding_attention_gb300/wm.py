@@ -63,6 +63,9 @@ def library_path() -> str:
 def load() -> ctypes.CDLL:
     """Load libwm.so; raises if it was not built (``__graft_entry__.build()``)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded already: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
